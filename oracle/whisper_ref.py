@@ -1,0 +1,235 @@
+"""Plain CPU oracle of the Whisper audio-encoder forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's CPU-baseline /
+reference arm may import this module; the library never does, and this module imports
+nothing from the library.  It is deliberately slow and literal: every step is the plain
+definition of what the step computes, in float64, with a library primitive (a matrix
+product, erf, exp) as the only building block.  No FFT, no blocking, no fusion.
+
+Sources (web pages the method is described on; section names as they appear there):
+  [CKE]  "How Audio Becomes Words: Whisper's Kernels Step By Step On A CPU"
+         -- section "The Frontend: Sound Becomes A Tensor" (the eight front-end kernels and
+            the bullets that walk them), "The Encoder: Understand Once",
+            "The Full Stitched Circuit", "Tiny, Base, Small, Large".
+  [API]  "whisper 0.9.0 API" -- model.nu (encoder shape, k_proj without bias, wh_encode
+         layouts) and kernels.nu (LayerNorm with bias, erf GELU, conv1d, non-causal
+         attention with the 1/sqrt(hd) score scale).
+
+Readings where the pages are silent (each is a decision, recorded with the code):
+  r1  3000 frames: centred, reflect-padded frames t = 0..2999 (the 3001st is dropped).
+  r2  reflect = mirror without repeating the edge sample (x[-1] = x[1]).
+  r3  Hann is periodic: 0.5 - 0.5 cos(2 pi n / 400).
+  r4  power = re^2 + im^2.
+  r5  Slaney mel scale, M+2 points equally spaced in mel over [0, 8000] Hz, triangles
+      area-normalised by 2 / (f[m+2] - f[m]), evaluated at bin frequencies 40 k Hz.
+  r6  log floor 1e-10 inside log10.
+  r7  the "global" maximum is per window (per 30-s clip).
+  r8  clamp at (max - 8) in log10 units, i.e. -80 dB of power.
+  r9  conv padding is zeros.
+  r10 LayerNorm eps 1e-5, biased variance.
+  r11 GELU is the exact erf form.
+  r12 scores scaled by 1/sqrt(64); head h owns columns [64 h, 64 h + 64).
+  r13 GELU after each conv; positions added after conv2's GELU.
+
+Pinned by tests/test_oracle_*.py against closed forms, invariants, library routines
+(numpy.fft, torch.stft, torch.nn.functional) and brute force.  The full encoder has no
+published value to pin it: it is pinned by an independent restatement with torch CPU ops.
+"""
+import numpy as np
+from scipy.special import erf
+
+SAMPLE_RATE = 16_000
+N_SAMPLES = 480_000
+N_FFT = 400
+HOP = 160
+N_FRAMES = 3000
+N_BINS = N_FFT // 2 + 1      # 201
+N_CTX = 1500
+HEAD_DIM = 64
+LN_EPS = 1e-5
+LOG_FLOOR = 1e-10
+
+
+# ========================================================================================
+# Front end  [CKE] "The Frontend: Sound Becomes A Tensor", kernels 3-6 and their bullets
+# ========================================================================================
+def pad_or_truncate(pcm: np.ndarray, n_samples: int = N_SAMPLES) -> np.ndarray:
+    """Kernel 3 'pad or truncate': zero-pad short clips, cut long ones, to 480000 samples."""
+    x = np.zeros(n_samples, dtype=np.float64)
+    m = min(len(pcm), n_samples)
+    x[:m] = pcm[:m]
+    return x
+
+
+def hann_periodic(n_fft: int = N_FFT) -> np.ndarray:
+    """Kernel 4 'periodic Hann' (r3): w[n] = 0.5 - 0.5 cos(2 pi n / N), n = 0..N-1."""
+    n = np.arange(n_fft, dtype=np.float64)
+    return 0.5 - 0.5 * np.cos(2.0 * np.pi * n / n_fft)
+
+
+def frame_signal(x: np.ndarray) -> np.ndarray:
+    """Kernel 4 'reflect-pad' and framing (r1, r2): frame t holds samples
+    160 t - 200 .. 160 t + 199 of x, an index i < 0 reading x[-i] and an index i > N-1
+    reading x[2 (N-1) - i].  Returns float64 [3000][400]."""
+    n = len(x)
+    half = N_FFT // 2
+    t = np.arange(N_FRAMES)[:, None]
+    j = np.arange(N_FFT)[None, :]
+    i = HOP * t + j - half
+    i = np.where(i < 0, -i, i)
+    i = np.where(i > n - 1, 2 * (n - 1) - i, i)
+    return x[i].astype(np.float64)
+
+
+def dft_power(frames: np.ndarray, window: np.ndarray) -> np.ndarray:
+    """Kernel 4 'STFT power' (r4): P[t][k] = |sum_n w[n] frame_t[n] exp(-2 pi i k n / 400)|^2
+    for k = 0..200, by the direct definition (a float64 matrix product, no FFT)."""
+    n = np.arange(N_FFT, dtype=np.float64)[:, None]
+    k = np.arange(N_BINS, dtype=np.float64)[None, :]
+    ang = 2.0 * np.pi * ((n * k) % N_FFT) / N_FFT      # reduce n k mod N before the angle
+    xw = frames * window[None, :]
+    re = xw @ np.cos(ang)
+    im = -(xw @ np.sin(ang))
+    return re * re + im * im
+
+
+def hz_to_mel_slaney(f):
+    """Slaney mel scale (r5): linear below 1 kHz (3 f / 200), logarithmic above,
+    with 27 mel per factor 6.4 in frequency."""
+    f = np.asarray(f, dtype=np.float64)
+    lin = 3.0 * f / 200.0
+    logpart = 15.0 + 27.0 * np.log(np.maximum(f, 1e-300) / 1000.0) / np.log(6.4)
+    return np.where(f < 1000.0, lin, logpart)
+
+
+def mel_to_hz_slaney(m):
+    m = np.asarray(m, dtype=np.float64)
+    lin = 200.0 * m / 3.0
+    logpart = 1000.0 * np.exp((m - 15.0) * np.log(6.4) / 27.0)
+    return np.where(m < 15.0, lin, logpart)
+
+
+def mel_filterbank(n_mels: int, sr: int = SAMPLE_RATE, n_fft: int = N_FFT) -> np.ndarray:
+    """Kernel 5 'mel filters': n_mels triangles on the Slaney scale, area-normalised (r5).
+    Returns float64 [n_mels][201]."""
+    edges_mel = np.linspace(hz_to_mel_slaney(0.0), hz_to_mel_slaney(sr / 2.0), n_mels + 2)
+    f = mel_to_hz_slaney(edges_mel)                                 # [n_mels + 2] Hz
+    bins = np.arange(n_fft // 2 + 1, dtype=np.float64) * sr / n_fft  # 40 Hz apart
+    fb = np.zeros((n_mels, len(bins)))
+    for m in range(n_mels):
+        lo, c, hi = f[m], f[m + 1], f[m + 2]
+        rising = (bins - lo) / (c - lo)
+        falling = (hi - bins) / (hi - c)
+        fb[m] = np.maximum(0.0, np.minimum(rising, falling)) * (2.0 / (hi - lo))
+    return fb
+
+
+def log_mel_from_power(power: np.ndarray, fb: np.ndarray) -> np.ndarray:
+    """Kernels 5-6: mel projection, log10 with floor (r6), clamp at the window maximum
+    minus 8 (r7, r8), then (x + 4) / 4.  power [3000][201] -> [3000][n_mels] (frame-major)."""
+    s = power @ fb.T
+    lg = np.log10(np.maximum(s, LOG_FLOOR))
+    lg = np.maximum(lg, lg.max() - 8.0)
+    return (lg + 4.0) / 4.0
+
+
+def log_mel(pcm: np.ndarray, n_mels: int) -> np.ndarray:
+    """One window: pcm (any length, 16 kHz) -> log-mel float32 [3000][n_mels], a frame
+    contiguous ([API] wh_encode: 'mel is 3000 x n_mels, row-major')."""
+    x = pad_or_truncate(np.asarray(pcm, dtype=np.float64))
+    p = dft_power(frame_signal(x), hann_periodic())
+    return log_mel_from_power(p, mel_filterbank(n_mels)).astype(np.float32)
+
+
+# ========================================================================================
+# Encoder  [API] model.nu and kernels.nu; [CKE] "The Encoder", "The Full Stitched Circuit"
+# ========================================================================================
+def gelu(x: np.ndarray) -> np.ndarray:
+    """[API] kernels.nu: GELU with the error function (r11): x * Phi(x)."""
+    return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+
+
+def layer_norm(x: np.ndarray, g: np.ndarray, b: np.ndarray, eps: float = LN_EPS) -> np.ndarray:
+    """[API] kernels.nu: LayerNorm subtracts the mean and has a bias (r10, biased variance)."""
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * g + b
+
+
+def conv1d_k3(x: np.ndarray, w: np.ndarray, b: np.ndarray, stride: int) -> np.ndarray:
+    """[API] model.nu conv1/conv2: kernel 3, padding 1 (zeros, r9), stride 1 or 2.
+    x [T_in][C_in] (time-major), w [C_out][C_in][3] -> [T_out][C_out] with
+    y[t][o] = b[o] + sum_{i, j} w[o][i][j] x[stride t + j - 1][i].  Written as an explicit
+    im2col (column index i * 3 + j, matching w's flattening) and one matrix product."""
+    t_in, c_in = x.shape
+    t_out = (t_in + 2 - 3) // stride + 1
+    xp = np.zeros((t_in + 2, c_in), dtype=np.float64)
+    xp[1:-1] = x
+    cols = np.empty((t_out, c_in, 3), dtype=np.float64)
+    for j in range(3):
+        cols[:, :, j] = xp[j: j + stride * (t_out - 1) + 1: stride]
+    return cols.reshape(t_out, c_in * 3) @ w.reshape(w.shape[0], c_in * 3).T.astype(np.float64) + b
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_head: int, return_probs=False):
+    """[API] kernels.nu attn_sc / attn_out and [CKE] "The Encoder": NON-causal attention, the
+    full T x T square, scores q.k / sqrt(64) (r12), softmax over all keys, times v.
+    q, k, v: [T][n_head * 64] -> [T][n_head * 64]."""
+    t, d = q.shape
+    hd = d // n_head
+    out = np.empty((t, d), dtype=np.float64)
+    probs = []
+    for h in range(n_head):
+        sl = slice(h * hd, (h + 1) * hd)
+        s = (q[:, sl] @ k[:, sl].T) / np.sqrt(hd)
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=1, keepdims=True)
+        out[:, sl] = p @ v[:, sl]
+        if return_probs:
+            probs.append(p)
+    return (out, probs) if return_probs else out
+
+
+def _f64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def encoder_block(x: np.ndarray, lw: dict, n_head: int, bk=None) -> np.ndarray:
+    """[API] model.nu: x += out_proj(attn(LN1(x))); x += fc2(GELU(fc1(LN2(x)))).
+    q, v and out_proj have biases; k_proj has none (bk only exists so a test can show that
+    a k bias cannot change the result)."""
+    h = layer_norm(x, _f64(lw["ln1_g"]), _f64(lw["ln1_b"]))
+    q = h @ _f64(lw["wq"]).T + _f64(lw["bq"])
+    k = h @ _f64(lw["wk"]).T
+    if bk is not None:
+        k = k + _f64(bk)
+    v = h @ _f64(lw["wv"]).T + _f64(lw["bv"])
+    a = attention(q, k, v, n_head)
+    x = x + a @ _f64(lw["wo"]).T + _f64(lw["bo"])
+    h = layer_norm(x, _f64(lw["ln2_g"]), _f64(lw["ln2_b"]))
+    h = gelu(h @ _f64(lw["w1"]).T + _f64(lw["b1"]))
+    return x + h @ _f64(lw["w2"]).T + _f64(lw["b2"])
+
+
+def encoder_stem(mel: np.ndarray, w: dict) -> np.ndarray:
+    """[API] model.nu, [CKE] kernel 7-8: GELU(conv1) -> GELU(conv2, stride 2) -> + stored
+    positions (r13).  mel [3000][n_mels] -> x [1500][d]."""
+    c1 = gelu(conv1d_k3(_f64(mel), _f64(w["conv1_w"]), _f64(w["conv1_b"]), 1))
+    c2 = gelu(conv1d_k3(c1, _f64(w["conv2_w"]), _f64(w["conv2_b"]), 2))
+    return c2 + _f64(w["pos"])[: c2.shape[0]]
+
+
+def encoder(mel: np.ndarray, w: dict, n_head: int) -> np.ndarray:
+    """The whole encoder for one window: stem, N blocks, final LayerNorm.
+    Returns float64 [1500][d] (the memory the decoder attends to)."""
+    x = encoder_stem(mel, w)
+    for lw in w["layers"]:
+        x = encoder_block(x, lw, n_head)
+    return layer_norm(x, _f64(w["lnf_g"]), _f64(w["lnf_b"]))
+
+
+def encode_window(pcm: np.ndarray, w: dict, n_mels: int, n_head: int):
+    """Front end + encoder for one window: returns (log-mel float32, encoder output float64)."""
+    mel = log_mel(pcm, n_mels)
+    return mel, encoder(mel, w, n_head)
