@@ -1,0 +1,319 @@
+#!/usr/bin/env python
+"""Whisper audio-encoder benchmark: 30-s windows/s on one GB300 (or N replicas).
+
+One step = one pass of the whole path over one batch: wh_frontend (PCM -> log-mel) and
+wh_encode (conv stem, every encoder block, final LayerNorm), inputs resident in HBM.
+Default workload: the large-v3-shaped encoder (128 mels, d 1280, 20 heads, 32 blocks,
+ffn 5120) over a batch of 16 synthetic speech-like 30-s windows, random N(0, 0.02) bf16
+weights.  Every step's working set (1.27 GB of weights, ~0.7 GB of activations) is far
+larger than the 129 MB L2, so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config IDX] [--impl reference]
+
+Multi-GPU: torchrun, one process per GPU; each rank encodes its own windows (no collective
+on the data path, weak scaling); the barrier and the max over ranks are for timing only.
+--impl reference times the CPU oracle (plain float64 NumPy) on a bounded sample instead.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "encoder 30-s windows/sec (1 GB300) and fraction of BF16 tensor-core peak"
+DEFAULT_CONFIG = 4
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _workload(cfg, n_gpus):
+    return {"workload": f"{cfg.name}: {cfg.batch} x 30-s 16 kHz windows per GPU, {cfg.n_mels} mels, "
+                        f"d_model {cfg.d_model}, {cfg.n_head} heads, {cfg.n_layer} blocks, ffn {cfg.d_ff}, "
+                        f"1500 positions",
+            "batch_per_gpu": cfg.batch, "global_batch": cfg.batch * n_gpus, "seq_len": 1500,
+            "parallelism": f"replicas x{n_gpus} (windows sharded, no collective)",
+            "l2": "working set > L2 (weights + activations per step), no flush"}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle sample: window 0 -- front end, conv stem, ONE encoder block, final norm.
+# Blocks have identical shapes, so the window's time is fe + stem + n_layer * block + lnf.
+# ---------------------------------------------------------------------------------------
+def _oracle_sample(cfg, reps=1):
+    import numpy as np
+
+    from oracle import whisper_ref as R
+    from whisper_audio_encoder_gb300 import synth
+
+    pcm = synth.waveform(cfg, 0)
+    w = synth.weights(cfg, layers=[0])
+    best = None
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        mel = R.log_mel(pcm, cfg.n_mels)
+        t1 = time.perf_counter()
+        x = R.encoder_stem(mel, w)
+        t2 = time.perf_counter()
+        x = R.encoder_block(x, w["layers"][0], cfg.n_head)
+        t3 = time.perf_counter()
+        R.layer_norm(x, np.asarray(w["lnf_g"], np.float64), np.asarray(w["lnf_b"], np.float64))
+        t4 = time.perf_counter()
+        per_window = (t1 - t0) + (t2 - t1) + cfg.n_layer * (t3 - t2) + (t4 - t3)
+        best = per_window if best is None else min(best, per_window)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"window 0 of {cfg.name}: oracle front end, conv stem, 1 of {cfg.n_layer} blocks and final "
+              f"LayerNorm (float64 NumPy, BLAS threads = host cores); window time = fe + stem + "
+              f"{cfg.n_layer} x block + norm, best of {reps}")
+    return 1.0 / best, cores, sample
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from whisper_audio_encoder_gb300 import configs
+    cfg = configs.CONFIGS[args.config]
+    for _ in range(args.warmup):
+        _oracle_sample(cfg)
+    vals = [_oracle_sample(cfg)[0] for _ in range(args.steps)]
+    v, cores, sample = _oracle_sample(cfg)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _workload(cfg, 1),
+            "cpu_baseline": {"value": value, "unit": "windows/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "windows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx = float(f[2])
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _traffic_from_profiles(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary (or None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        return json.load(fh).get(kernel)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from whisper_audio_encoder_gb300 import build, configs, synth, wh
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    wh.lib()
+    cfg = configs.CONFIGS[args.config]
+    B = cfg.batch
+    weights = synth.weights(cfg)
+    enc = wh.Encoder(cfg, weights, device=f"cuda:{local}")
+    del weights
+    pcm_np = synth.waveforms(cfg, windows=range(rank * B, rank * B + B))
+    pcm_h = torch.from_numpy(pcm_np).pin_memory()
+    pcm_d = pcm_h.cuda()
+    mel_d = torch.empty(B, 3000, cfg.n_mels, device="cuda")
+    out_d = torch.empty(B, 1500, cfg.d_model, device="cuda")
+    out_h = torch.empty(B, 1500, cfg.d_model).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        enc.forward(pcm_d, mel=mel_d, out=out_d)
+    torch.cuda.synchronize()
+    st = wh.wh_status()
+    if st != wh.WH_OK:
+        raise RuntimeError(f"device status after warm-up: {wh.wh_strerror(st)}")
+
+    # ---- timed region: resident inputs
+    wh.wh_launch_count()
+    wh.wh_trace_enable(True)
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        enc.forward(pcm_d, mel=mel_d, out=out_d)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    launches = wh.wh_launch_count()
+    stats = wh.wh_trace_read()
+    wh.wh_trace_enable(False)
+    ms = e0.elapsed_time(e1) / args.steps
+
+    # ---- end to end through the public API: pinned host PCM in, memory out, every step
+    e2e_ms = None
+    if not args.no_e2e:
+        enc.encode_from_host(pcm_h, out_h, pcm_d, mel_d, out_d)
+        torch.cuda.synchronize()
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            enc.encode_from_host(pcm_h, out_h, pcm_d, mel_d, out_d)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    if dist is not None:
+        t = torch.tensor([ms, e2e_ms or 0.0], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), (float(t[1]) if e2e_ms is not None else None)
+    st = wh.wh_status()
+    if st != wh.WH_OK:
+        raise RuntimeError(f"device status after the timed region: {wh.wh_strerror(st)}")
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    peaks = _peaks()
+    value = B * ws * 1000.0 / ms
+    flops_window = cfg.flops_per_window()["total"]
+    g = stats.get("gemm", {"launches": 0, "total_ms": 0.0, "flops": 0.0})
+    gemm_avg_ms = g["total_ms"] / max(1, g["launches"])
+    gemm_flops_launch = g["flops"] / max(1, g["launches"])
+    achieved = gemm_flops_launch / (gemm_avg_ms * 1e-3) / 1e12 if gemm_avg_ms > 0 else 0.0
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = _traffic_from_profiles("gemm")
+    kernels = {k: {"launches": v["launches"], "ms_per_step": v["total_ms"] / args.steps,
+                   "share": v["total_ms"] / max(1e-9, sum(s["total_ms"] for s in stats.values())),
+                   **({"tflops": v["flops"] / (v["total_ms"] * 1e-3) / 1e12} if v["flops"] > 0 else {}),
+                   **({"gbs": v["bytes"] / (v["total_ms"] * 1e-3) / 1e9} if v["flops"] == 0 else {})}
+               for k, v in stats.items()}
+    line = {
+        "metric": METRIC, "value": value, "unit": "windows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded speech-like waveforms, random weights)",
+        "config": _workload(cfg, ws),
+        "encoder_tflops": flops_window * B * ws / (ms * 1e-3) / 1e12,
+        "frac_of_bf16_peak": flops_window * B / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
+        "roofline": {"bound": "tensor", "kernel": "gemm (tcgen05, all encoder dense layers)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{peaks['source']} bf16 sustained", "traffic": traffic},
+        "kernels": kernels,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if e2e_ms is not None:
+        line["e2e"] = {"value": B * ws * 1000.0 / e2e_ms, "unit": "windows/s",
+                       "h2d_bytes_per_step": int(pcm_h.numel() * 4), "d2h_bytes_per_step": int(out_h.numel() * 4)}
+    if ws == 1 and not args.no_cpu_baseline:
+        v, cores, sample = _oracle_sample(cfg)
+        line["cpu_baseline"] = {"value": v, "unit": "windows/s", "cores": cores, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

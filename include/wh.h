@@ -1,0 +1,182 @@
+/*
+ * wh.h -- C ABI of libwh.so: the Whisper audio-encoder forward pass on one GB300 (sm_103a).
+ *
+ * The path: 16 kHz PCM -> log-mel (wh_frontend) -> conv stem + N pre-LN encoder blocks +
+ * final LayerNorm (wh_encode) -> the 1500 x d_model memory the decoder attends to.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise.  The caller owns every
+ *     buffer (inputs, outputs, weights, workspace); the library never frees or keeps them.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL = the legacy
+ *     default stream).  Argument errors are detected on the host and returned before anything
+ *     is launched.  Errors found on the device (a bounded wait that ran out, a bounds check)
+ *     are recorded in a per-device status word and returned by wh_status().
+ *   - The library's own persistent state is small constant tables (Hann window, twiddles,
+ *     mel filterbanks) in __constant__ memory, set up on the first call on each device.
+ *     Make that first call outside any CUDA-graph capture.
+ *   - Matrices are bfloat16 (passed as wh_bf16 bit patterns), vectors are float32,
+ *     accumulation is float32, the residual stream is float32.
+ *   - Return value: WH_OK (0) or one of the WH_E* codes below; wh_strerror() names them.
+ */
+#ifndef WH_H
+#define WH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    WH_OK = 0,
+    WH_EINVAL = 1,     /* bad argument: null pointer, unsupported shape, misaligned buffer */
+    WH_ENOSPC = 2,     /* workspace smaller than the matching *_workspace() size */
+    WH_ECUDA = 3,      /* a CUDA runtime call or launch failed */
+    WH_ETIMEOUT = 4,   /* a device-side bounded wait ran out (reported by wh_status) */
+    WH_EBOUNDS = 5,    /* a device-side bounds check fired (reported by wh_status) */
+    WH_ENODEV = 6      /* no usable CUDA device */
+};
+
+typedef uint16_t wh_bf16;   /* bfloat16 bit pattern */
+
+/* Encoder hyper-parameters ("whisper 0.9.0 API", model.nu: the shape is read from the
+ * checkpoint, not hard-coded).  head_dim = d_model / n_head must be 64; n_mels is 80 or 128
+ * ("How Audio Becomes Words", section "Tiny, Base, Small, Large": large-v3 uses 128 bins);
+ * d_model and d_ff multiples of 128, d_model <= 2048.  n_layer may be 0 (stem + final norm).
+ * The encoder context is fixed at 1500 positions. */
+typedef struct {
+    int n_mels, d_model, n_head, n_layer, d_ff;
+} wh_config;
+
+/* One encoder block ("whisper 0.9.0 API", model.nu: N x [LN -> self-attn -> +residual,
+ * LN -> fc1 -> GELU -> fc2 -> +residual]).  Matrices use the nn.Linear layout [out][in],
+ * row-major.  q, v and out_proj have a bias; k_proj has NONE (model.nu: "k_proj HAS NO
+ * BIAS"), so there is no bk field. */
+typedef struct {
+    const float *ln1_g, *ln1_b;            /* [d] */
+    const wh_bf16 *wq, *wk, *wv;           /* [d][d] each */
+    const float *bq, *bv;                  /* [d] */
+    const wh_bf16 *wo;  const float *bo;   /* [d][d], [d] */
+    const float *ln2_g, *ln2_b;            /* [d] */
+    const wh_bf16 *w1;  const float *b1;   /* fc1: [d_ff][d], [d_ff] */
+    const wh_bf16 *w2;  const float *b2;   /* fc2: [d][d_ff], [d] */
+} wh_layer_weights;
+
+/* All encoder weights.  `layers` is a HOST array of n_layer structs (of device pointers).
+ * Conv weights use the PyTorch Conv1d layout [c_out][c_in][3] (the pages give no layout). */
+typedef struct {
+    const wh_bf16 *conv1_w; const float *conv1_b;   /* [d][n_mels][3], [d] */
+    const wh_bf16 *conv2_w; const float *conv2_b;   /* [d][d][3], [d] */
+    const float *pos;                               /* stored positions [1500][d] */
+    const wh_layer_weights *layers;                 /* host array [n_layer] */
+    const float *lnf_g, *lnf_b;                     /* final LayerNorm [d] */
+} wh_weights;
+
+/* ---------------------------------------------------------------------------------------
+ * Front end.  "How Audio Becomes Words", section "The Frontend: Sound Becomes A Tensor",
+ * kernels 3-6: pad or truncate to 480000 samples; reflect padding, periodic Hann(400),
+ * n_fft 400, hop 160 -> a 201 x 3000 power grid; Slaney mel filters (area-normalised) to
+ * n_mels bins; log10, a clamp at (window maximum - 8) (-80 dB, relative to the loudest
+ * point of the whole clip) and (x + 4) / 4.
+ *
+ *   pcm   device float32 [batch][n]: window b's samples start at pcm + b * n.  n >= 0;
+ *         n < 480000 reads zeros past the end, n > 480000 ignores the rest.
+ *   mel   device float32 [batch][3000][n_mels], a frame contiguous ("whisper 0.9.0 API",
+ *         wh_encode: "mel is 3000 x n_mels, row-major (a frame is contiguous)").
+ *   workspace  device scratch of at least wh_frontend_workspace(batch) bytes, 16-byte aligned
+ *         (the per-window maxima); contents need not be initialised.
+ * Errors: WH_EINVAL (null pointer with batch > 0, n < 0, batch < 0, n_mels not 80/128),
+ *         WH_ENOSPC (workspace too small), WH_ECUDA.  batch == 0 is a no-op.
+ * ------------------------------------------------------------------------------------ */
+size_t wh_frontend_workspace(int batch);
+int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel,
+                void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Encoder.  "whisper 0.9.0 API", model.nu: conv1 (k=3, s=1, pad=1) n_mels -> d, GELU;
+ * conv2 (k=3, s=2, pad=1) d -> d, GELU, 3000 -> 1500 frames; + stored positions; n_layer
+ * pre-LN blocks with NON-causal self-attention (scores q.k / sqrt(64), kernels.nu); final
+ * LayerNorm (eps 1e-5); GELU is the erf form (kernels.nu).
+ *
+ *   mel   device float32 [batch][3000][n_mels] (as produced by wh_frontend)
+ *   out   device float32 [batch][1500][d_model], row-major ("wh_enc_out: 1500 x d_model,
+ *         row-major"); may not alias mel or the workspace.
+ *   workspace  device scratch of at least wh_encode_workspace(cfg, batch) bytes, 256-byte
+ *         aligned; contents need not be initialised; not to be shared by concurrent calls.
+ * Errors: WH_EINVAL (null pointer, unsupported config, misaligned pointer), WH_ENOSPC,
+ *         WH_ECUDA.  batch == 0 is a no-op.
+ * ------------------------------------------------------------------------------------ */
+size_t wh_encode_workspace(const wh_config *cfg, int batch);
+int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weights *w,
+              float *out, void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Single steps of the encoder, exposed for testing and for callers that compose their own
+ * pipeline.  Same conventions as above.
+ * ------------------------------------------------------------------------------------ */
+
+/* LayerNorm ("whisper 0.9.0 API", kernels.nu: it subtracts the mean and has a bias):
+ * y[r] = (x[r] - mean) / sqrt(var + 1e-5) * g + b over d columns, biased variance.
+ * x float32 [rows][d]; y is bf16 (y_bf16 = 1) or float32 (y_bf16 = 0) [rows][d].
+ * d a multiple of 64, 64 <= d <= 2048. */
+int wh_layer_norm(const float *x, int rows, int d, const float *g, const float *b,
+                  void *y, int y_bf16, void *stream);
+
+/* Dense layer on the tensor cores: acc[r][c] = sum_k a[r][k] * w[c][k] (nn.Linear [out][in]).
+ * a bf16 [rows][k], w bf16 [n][k]; k a multiple of 8, n a multiple of 128.
+ *   WH_EPI_BF16        y bf16 [rows][n] = acc + bias
+ *   WH_EPI_GELU_BF16   y bf16 [rows][n] = GELU(acc + bias)      (fc1)
+ *   WH_EPI_RESID_F32   y float32 [rows][n] += acc + bias       (out_proj, fc2)
+ * bias may be NULL (no bias). */
+enum { WH_EPI_BF16 = 0, WH_EPI_GELU_BF16 = 1, WH_EPI_RESID_F32 = 2 };
+int wh_linear(const wh_bf16 *a, int rows, int k, const wh_bf16 *w, int n, const float *bias,
+              int epilogue, void *y, void *stream);
+
+/* Non-causal multi-head attention over all n_ctx keys ("whisper 0.9.0 API", kernels.nu,
+ * attn_f / attn_sc / attn_out with causal = 0): for each window b and head h,
+ * o = softmax(q k^T / sqrt(64)) v.  qkv bf16 [batch * n_ctx][3 * n_head * 64] with the q,
+ * k and v of head h in columns 64 h, D + 64 h and 2 D + 64 h (D = 64 n_head);
+ * out bf16 [batch * n_ctx][D].  1 <= n_ctx <= 1500. */
+int wh_attention(const wh_bf16 *qkv, int batch, int n_ctx, int n_head, wh_bf16 *out,
+                 void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Status, errors, tracing
+ * ------------------------------------------------------------------------------------ */
+
+/* Synchronises `stream`, then returns and clears the current device's status word:
+ * WH_OK, WH_ETIMEOUT or WH_EBOUNDS (or WH_ECUDA if the synchronisation failed). */
+int wh_status(void *stream);
+
+/* A static, NUL-terminated name for a WH_* code. */
+const char *wh_strerror(int code);
+
+/* Self-test of the bounded-wait machinery: launches one block that waits on a barrier that
+ * nothing completes, with a wait limit of `limit_ns` nanoseconds (<= 1e9).  The wait runs
+ * out, the block records WH_ETIMEOUT in the status word and returns; wh_status() then
+ * reports it.  Does not fault or hang the GPU. */
+int wh_selftest_timeout(uint64_t limit_ns, void *stream);
+
+/* Per-kernel timing with CUDA events recorded around each launch on the launching stream.
+ * wh_trace_enable(1) starts recording (clearing earlier records), 0 stops.  wh_trace_read
+ * synchronises the recorded events and fills up to `max` entries (one per kernel class)
+ * with launch counts, total device milliseconds and algorithmic work; returns the number of
+ * classes, or a negative WH_E* code. */
+typedef struct {
+    char name[32];        /* kernel class: "gemm", "attention", "layernorm", "frontend", ... */
+    int launches;
+    double total_ms;
+    double flops;         /* algorithmic flops of all recorded launches */
+    double bytes;         /* algorithmic HBM bytes of all recorded launches */
+} wh_trace_stat;
+int wh_trace_enable(int on);
+int wh_trace_read(wh_trace_stat *out, int max);
+
+/* Number of kernels the library launched since the last call (all devices, all streams). */
+int64_t wh_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WH_H */

@@ -1,0 +1,113 @@
+"""The C-ABI library loads, exports every symbol include/wh.h declares, and rejects bad
+arguments on the host before touching a device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from whisper_audio_encoder_gb300 import build, wh
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wh.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return wh.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wh_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ("wh_frontend", "wh_frontend_workspace", "wh_encode", "wh_encode_workspace", "wh_status",
+                 "wh_strerror"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in _declared() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_strerror_names_every_code(L):
+    for code in range(7):
+        assert wh.wh_strerror(code).startswith("WH_")
+    assert "unknown" in wh.wh_strerror(99)
+
+
+def test_workspace_sizes(L):
+    cfg = wh.wh_config(80, 384, 6, 4, 1536)
+    one = L.wh_encode_workspace(ctypes.byref(cfg), 1)
+    assert one > 0 and L.wh_encode_workspace(ctypes.byref(cfg), 8) > 7 * one
+    assert L.wh_frontend_workspace(0) == 0 and L.wh_frontend_workspace(5) >= 20
+    bad = wh.wh_config(81, 384, 6, 4, 1536)
+    assert L.wh_encode_workspace(ctypes.byref(bad), 1) == 0
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("cfg", [(81, 384, 6, 1, 1536), (80, 384, 5, 1, 1536), (80, 320, 5, 1, 1280),
+                                 (80, 384, 6, -1, 1536), (80, 384, 6, 1, 100), (128, 4096, 64, 1, 4096)])
+def test_encode_rejects_unsupported_configs(L, cfg):
+    c = wh.wh_config(*cfg)
+    w = wh.wh_weights()
+    assert L.wh_encode(FAKE, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+
+
+def test_encode_rejects_null_weights_and_small_workspace(L):
+    c = wh.wh_config(80, 384, 6, 0, 1536)
+    w = wh.wh_weights()                                   # all NULL
+    assert L.wh_encode(FAKE, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+    assert L.wh_encode(None, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+    w = wh.wh_weights(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE)
+    assert L.wh_encode(FAKE, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 16, None) == wh.WH_ENOSPC
+    c.n_layer = 1                                           # layers array missing
+    assert L.wh_encode(FAKE, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+    assert L.wh_encode(FAKE, 0, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 0, None) == wh.WH_OK  # batch 0
+
+
+def test_encode_rejects_misaligned_pointers(L):
+    c = wh.wh_config(80, 384, 6, 0, 1536)
+    w = wh.wh_weights(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert L.wh_encode(odd, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+    w.pos = odd
+    assert L.wh_encode(FAKE, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+
+
+def test_frontend_rejects_bad_arguments(L):
+    assert L.wh_frontend(FAKE, 480000, 1, 81, FAKE, FAKE, 256, None) == wh.WH_EINVAL
+    assert L.wh_frontend(FAKE, -1, 1, 80, FAKE, FAKE, 256, None) == wh.WH_EINVAL
+    assert L.wh_frontend(FAKE, 480000, -1, 80, FAKE, FAKE, 256, None) == wh.WH_EINVAL
+    assert L.wh_frontend(None, 480000, 1, 80, FAKE, FAKE, 256, None) == wh.WH_EINVAL
+    assert L.wh_frontend(FAKE, 480000, 1, 80, None, FAKE, 256, None) == wh.WH_EINVAL
+    assert L.wh_frontend(FAKE, 480000, 1, 80, FAKE, None, 256, None) == wh.WH_EINVAL
+    assert L.wh_frontend(FAKE, 480000, 100, 80, FAKE, FAKE, 16, None) == wh.WH_ENOSPC
+    assert L.wh_frontend(None, 480000, 0, 80, None, None, 0, None) == wh.WH_OK          # batch 0
+
+
+def test_single_step_entry_points_reject_bad_shapes(L):
+    assert L.wh_layer_norm(FAKE, 4, 100, FAKE, FAKE, FAKE, 1, None) == wh.WH_EINVAL   # d % 64
+    assert L.wh_layer_norm(FAKE, 4, 4096, FAKE, FAKE, FAKE, 1, None) == wh.WH_EINVAL  # d > 2048
+    assert L.wh_linear(FAKE, 4, 60, FAKE, 128, None, 0, FAKE, None) == wh.WH_EINVAL    # k % 8
+    assert L.wh_linear(FAKE, 4, 64, FAKE, 100, None, 0, FAKE, None) == wh.WH_EINVAL    # n % 128
+    assert L.wh_linear(FAKE, 4, 64, FAKE, 128, None, 7, FAKE, None) == wh.WH_EINVAL    # epilogue
+    assert L.wh_attention(FAKE, 1, 1501, 6, FAKE, None) == wh.WH_EINVAL                # n_ctx > 1500
+    assert L.wh_attention(FAKE, 1, 0, 6, FAKE, None) == wh.WH_EINVAL
+    assert L.wh_selftest_timeout(0, None) == wh.WH_EINVAL
+    assert L.wh_selftest_timeout(2_000_000_000, None) == wh.WH_EINVAL
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_no_device_is_reported(L):
+    assert L.wh_frontend(FAKE, 480000, 1, 80, FAKE, FAKE, 256, None) == wh.WH_ENODEV
+    assert L.wh_status(None) == wh.WH_ENODEV

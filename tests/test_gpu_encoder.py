@@ -1,0 +1,92 @@
+"""End-to-end parity: GPU front end + encoder (wh_frontend + wh_encode through the C ABI)
+against the oracle on the five workloads at their full batch sizes, compared window by
+window on sampled windows (the oracle runs one window at a time in float64).
+
+Bar: log-mel max-abs <= 1e-3; encoder output max-abs <= 3e-2 and every frame's cosine
+similarity >= 0.999."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import whisper_ref as R
+from whisper_audio_encoder_gb300 import build, configs, synth, wh
+
+from helpers import LOGMEL_ATOL, check_encoder, maxabs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    build.build()
+    wh.lib()
+
+
+
+@pytest.mark.parametrize("idx,windows", [(0, [0]), (1, [0, 2, 7]), (2, [0, 15]), (3, [0, 31]), (4, [0, 15])])
+def test_encoder_parity_on_workloads(idx, windows):
+    cfg = configs.CONFIGS[idx]
+    w = synth.weights(cfg)
+    enc = wh.Encoder(cfg, w)
+    pcm = synth.waveforms(cfg)
+    mel_d = wh.wh_frontend(torch.from_numpy(pcm).cuda(), cfg.n_mels)
+    out = enc.wh_encode(mel_d)
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    out = out.cpu().numpy()
+    mel = mel_d.cpu().numpy()
+    assert out.shape == (cfg.batch, 1500, cfg.d_model)
+    assert np.isfinite(out).all()
+    for win in windows:
+        mel_ref, out_ref = R.encode_window(pcm[win], w, cfg.n_mels, cfg.n_head)
+        assert maxabs(mel[win], mel_ref) <= LOGMEL_ATOL
+        check_encoder(out[win], out_ref, f"{cfg.name} window {win}")
+
+
+def test_encoder_with_random_layernorm_and_ragged_width():
+    """A non-Whisper width (d = 128, 2 heads, 128 mels) with random LayerNorm gamma/beta, so
+    a dropped or swapped LayerNorm parameter or a 128-wide tile path shows up."""
+    cfg = configs.EncoderConfig("test-d128", 128, 128, 2, 2, 512, 3, "speech", index=2)
+    w = synth.random_weights(128, 128, 2, 512, seed=21, ln_random=True)
+    enc = wh.Encoder(cfg, w)
+    pcm = synth.waveforms(cfg)
+    out = enc.forward(torch.from_numpy(pcm).cuda()).cpu().numpy()
+    for win in range(3):
+        _, ref = R.encode_window(pcm[win], w, 128, 2)
+        check_encoder(out[win], ref, f"window {win}")
+
+
+def test_stem_only_encoder():
+    """n_layer = 0: conv stem + positions + final LayerNorm."""
+    cfg = configs.EncoderConfig("stem-only", 80, 384, 6, 0, 1536, 2, "sines", index=1)
+    w = synth.random_weights(80, 384, 0, 1536, seed=4, ln_random=True)
+    enc = wh.Encoder(cfg, w)
+    mel = np.random.default_rng(2).uniform(-1, 1, (2, 3000, 80)).astype(np.float32)
+    out = enc.wh_encode(torch.from_numpy(mel).cuda()).cpu().numpy()
+    for b in range(2):
+        check_encoder(out[b], R.encoder(mel[b].astype(np.float64), w, 6), f"stem window {b}")
+
+
+def test_windows_are_independent():
+    """The same window at two batch positions gives bit-identical memories, and changing one
+    window does not change another (no cross-window leakage in any kernel)."""
+    cfg = configs.CONFIGS[1]
+    enc = wh.Encoder(cfg, synth.weights(cfg))
+    pcm = synth.waveforms(cfg, windows=[3, 4, 3, 5])
+    out1 = enc.forward(torch.from_numpy(pcm).cuda()).cpu().numpy()
+    assert np.array_equal(out1[0], out1[2])
+    pcm[1] *= 0.5
+    out2 = enc.forward(torch.from_numpy(pcm).cuda()).cpu().numpy()
+    assert np.array_equal(out1[0], out2[0]) and np.array_equal(out1[3], out2[3])
+    assert not np.array_equal(out1[1], out2[1])
+
+
+def test_encode_is_deterministic():
+    cfg = configs.CONFIGS[0]
+    enc = wh.Encoder(cfg, synth.weights(cfg))
+    mel = wh.wh_frontend(torch.from_numpy(synth.waveforms(cfg)).cuda(), 80)
+    a = enc.wh_encode(mel).cpu().numpy()
+    b = enc.wh_encode(mel).cpu().numpy()
+    assert np.array_equal(a, b)

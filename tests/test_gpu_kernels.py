@@ -1,0 +1,120 @@
+"""GPU parity of the single steps, called through the C ABI, against the oracle's
+definitions on the same seeded inputs: LayerNorm, the tcgen05 dense layer with each fused
+epilogue (ragged row / K / N tails), non-causal attention with a peaked softmax, and the
+bounded-wait self-test (no fault, no hang: the status word reports the timeout)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import whisper_ref as R
+from whisper_audio_encoder_gb300 import build, wh
+
+from helpers import ATTN_ATOL, bf16_round_np, maxabs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    build.build()
+    wh.lib()
+
+
+def _dev(a, dtype=torch.float32):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dtype).cuda()
+
+
+@pytest.mark.parametrize("rows,d", [(1, 64), (37, 384), (300, 1280), (9, 2048), (1500, 512)])
+@pytest.mark.parametrize("out_bf16", [True, False])
+def test_layer_norm(rows, d, out_bf16):
+    rng = np.random.default_rng(rows * 7 + d)
+    x = (rng.standard_normal((rows, d)) * 2 + 0.5).astype(np.float32)
+    g = (1 + 0.2 * rng.standard_normal(d)).astype(np.float32)
+    b = (0.1 * rng.standard_normal(d)).astype(np.float32)
+    y = wh.wh_layer_norm(_dev(x), _dev(g), _dev(b), out_bf16=out_bf16)
+    torch.cuda.synchronize()
+    ref = R.layer_norm(x.astype(np.float64), g.astype(np.float64), b.astype(np.float64))
+    got = y.float().cpu().numpy()
+    if out_bf16:
+        assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
+    else:
+        assert maxabs(got, ref) < 2e-5
+    assert wh.wh_status() == wh.WH_OK
+
+
+LINEAR_SHAPES = [(1, 64, 128), (129, 240, 256), (300, 384, 384), (1500, 1280, 1280), (257, 1536, 512),
+                 (3000, 384, 1536)]
+
+
+@pytest.mark.parametrize("M,K,N", LINEAR_SHAPES)
+@pytest.mark.parametrize("epi", [wh.WH_EPI_BF16, wh.WH_EPI_GELU_BF16, wh.WH_EPI_RESID_F32])
+def test_linear(M, K, N, epi):
+    rng = np.random.default_rng(M + 3 * K + 7 * N + epi)
+    a = bf16_round_np(rng.standard_normal((M, K)))
+    w = bf16_round_np(rng.standard_normal((N, K)) * 0.05)
+    bias = (0.1 * rng.standard_normal(N)).astype(np.float32)
+    ref = a.astype(np.float64) @ w.astype(np.float64).T + bias
+    if epi == wh.WH_EPI_RESID_F32:
+        y0 = rng.standard_normal((M, N)).astype(np.float32)
+        y = _dev(y0)
+        wh.wh_linear(_dev(a, torch.bfloat16), _dev(w, torch.bfloat16), _dev(bias), epi, y=y)
+        torch.cuda.synchronize()
+        assert maxabs(y.cpu().numpy(), y0 + ref) < 1e-3
+    else:
+        if epi == wh.WH_EPI_GELU_BF16:
+            ref = R.gelu(ref)
+        y = wh.wh_linear(_dev(a, torch.bfloat16), _dev(w, torch.bfloat16), _dev(bias), epi)
+        torch.cuda.synchronize()
+        got = y.float().cpu().numpy()
+        bad = np.abs(got - ref) > 2.0 ** -8 * np.abs(ref) + 1e-3
+        assert not bad.any(), f"{bad.sum()} of {bad.size} outside tolerance, max {maxabs(got, ref)}"
+    assert wh.wh_status() == wh.WH_OK
+
+
+def test_linear_without_bias():
+    rng = np.random.default_rng(5)
+    a = bf16_round_np(rng.standard_normal((200, 128)))
+    w = bf16_round_np(rng.standard_normal((256, 128)) * 0.1)
+    y = wh.wh_linear(_dev(a, torch.bfloat16), _dev(w, torch.bfloat16), None, wh.WH_EPI_BF16)
+    torch.cuda.synchronize()
+    ref = a.astype(np.float64) @ w.astype(np.float64).T
+    assert np.all(np.abs(y.float().cpu().numpy() - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-3)
+
+
+@pytest.mark.parametrize("batch,n_ctx,n_head", [(1, 1, 1), (2, 64, 3), (1, 100, 2), (2, 1500, 2), (1, 1499, 6)])
+def test_attention_peaked_softmax(batch, n_ctx, n_head):
+    """q, k ~ N(0, 1): the softmax is peaked, so a wrong score, scale or mask shows."""
+    rng = np.random.default_rng(batch * 1000 + n_ctx + n_head)
+    D = 64 * n_head
+    qkv = bf16_round_np(rng.standard_normal((batch * n_ctx, 3 * D)))
+    out = wh.wh_attention(_dev(qkv, torch.bfloat16), batch, n_ctx, n_head)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy()
+    for b in range(batch):
+        blk = qkv[b * n_ctx:(b + 1) * n_ctx].astype(np.float64)
+        ref = R.attention(blk[:, :D], blk[:, D:2 * D], blk[:, 2 * D:], n_head)
+        assert maxabs(got[b * n_ctx:(b + 1) * n_ctx], ref) <= ATTN_ATOL
+
+
+def test_attention_is_not_causal():
+    rng = np.random.default_rng(17)
+    n_ctx, D = 256, 64
+    qkv = bf16_round_np(rng.standard_normal((n_ctx, 3 * D)))
+    o1 = wh.wh_attention(_dev(qkv, torch.bfloat16), 1, n_ctx, 1).float().cpu().numpy()
+    qkv2 = qkv.copy()
+    qkv2[-1, 2 * D:] += 8.0           # change the value of the LAST frame
+    o2 = wh.wh_attention(_dev(qkv2, torch.bfloat16), 1, n_ctx, 1).float().cpu().numpy()
+    assert np.max(np.abs(o1[0] - o2[0])) > 1e-4   # frame 0 sees the future
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    assert wh.wh_status() == wh.WH_OK
+    wh.wh_selftest_timeout(2_000_000)            # 2 ms limit on a barrier nothing completes
+    assert wh.wh_status() == wh.WH_ETIMEOUT
+    assert wh.wh_status() == wh.WH_OK            # cleared by the read
+    x = torch.ones(4, 64, device="cuda")
+    y = wh.wh_layer_norm(x, torch.ones(64, device="cuda"), torch.zeros(64, device="cuda"), out_bf16=False)
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)

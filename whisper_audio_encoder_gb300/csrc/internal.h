@@ -1,0 +1,53 @@
+// Host-side interfaces between the translation units of libwh.so (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace wh {
+
+struct DevCtl;
+
+// ---- GEMM (gemm_tc.cu) -----------------------------------------------------------------
+enum GemmMode {
+    GEMM_BF16 = 0,        // y bf16 = acc + bias[segment]
+    GEMM_GELU_BF16 = 1,   // y bf16 = GELU(acc + bias)
+    GEMM_RESID_F32 = 2,   // y f32 += acc + bias
+    GEMM_CONV1 = 3,       // GELU(acc + bias) scattered as bf16 into conv2's im2col matrix
+    GEMM_CONV2 = 4,       // y f32 = GELU(acc + bias) + pos[row % rows_per_win]
+};
+
+struct GemmDesc {
+    const void *a; int lda;               // bf16 [M][lda], K columns used
+    const void *b[3]; int ldb;            // bf16 [seg_n][ldb] per segment (K columns used)
+    int M, N, K, seg_n;                   // N = n_seg * seg_n
+    const float *bias[3];                 // per segment, nullable
+    void *out; long long ldo;             // output (elements)
+    const float *pos;                     // GEMM_CONV2: [rows_per_win][N]
+    int rows_per_win;                     // GEMM_CONV1: c1 frames per window; GEMM_CONV2: positions
+};
+// Returns a WH_* code.  Encodes the tensor maps and launches the persistent tcgen05 kernel.
+int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cudaStream_t s);
+
+// ---- front end (frontend.cu) -------------------------------------------------------------
+int frontend_init_tables();   // once per device (current device)
+int frontend_launch(const float *pcm, int64_t n, int batch, int n_mels, float *mel, uint32_t *wmax,
+                    cudaStream_t s);
+
+// ---- other kernels ---------------------------------------------------------------------
+int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,
+                     cudaStream_t s);
+int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, cudaStream_t s);
+int stem_im2col_launch(const float *mel, int batch, int n_mels, void *a1, cudaStream_t s);
+int pack_conv_weight_launch(const void *w, int c_out, int c_in, void *wp, cudaStream_t s);
+int selftest_timeout_launch(const DevCtl &ctl, cudaStream_t s);
+
+// ---- tracing (wh_api.cu) ------------------------------------------------------------------
+// Kernel classes for the per-kernel timing.
+enum TraceClass { TR_FRONTEND = 0, TR_STEM_PREP, TR_GEMM, TR_ATTN, TR_LAYERNORM, TR_NCLASS };
+void trace_begin(int cls, cudaStream_t s);
+void trace_end(int cls, cudaStream_t s, double flops, double bytes);
+void count_launch(int n = 1);
+
+}  // namespace wh

@@ -1,0 +1,74 @@
+// LayerNorm ("whisper 0.9.0 API", kernels.nu: LayerNorm, not RMSNorm -- it subtracts the
+// mean and it has a bias): y = (x - mean) / sqrt(var + 1e-5) * g + b, biased variance.
+// One warp per row, the row held in registers (d <= 2048: <= 32 float2 per lane), two
+// passes over the registers (mean, then centred variance), warp-shuffle reductions.
+// HBM-bound: reads 4 d bytes and writes 2 d (bf16) or 4 d (fp32) bytes per row.
+#include "common.cuh"
+#include "internal.h"
+
+namespace wh {
+
+namespace {
+
+constexpr int LN_THREADS = 256;
+constexpr int MAXV = 32;  // float2 per lane
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restrict__ x, int rows, int d,
+                                                          const float *__restrict__ g,
+                                                          const float *__restrict__ b, void *__restrict__ y) {
+    const int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int nv = d >> 6;
+    const float2 *xr = reinterpret_cast<const float2 *>(x + (long long)row * d);
+    float2 v[MAXV];
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i)
+        if (i < nv) {
+            v[i] = __ldg(xr + i * 32 + lane);
+            s += v[i].x + v[i].y;
+        }
+    const float mean = warp_sum(s) / (float)d;
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i)
+        if (i < nv) {
+            const float dx = v[i].x - mean, dy = v[i].y - mean;
+            q = fmaf(dx, dx, fmaf(dy, dy, q));
+        }
+    const float rstd = 1.0f / sqrtf(warp_sum(q) / (float)d + 1e-5f);
+    const float2 *g2 = reinterpret_cast<const float2 *>(g);
+    const float2 *b2 = reinterpret_cast<const float2 *>(b);
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i)
+        if (i < nv) {
+            const int c = i * 32 + lane;
+            const float2 gg = __ldg(g2 + c), bb = __ldg(b2 + c);
+            const float o0 = (v[i].x - mean) * rstd * gg.x + bb.x;
+            const float o1 = (v[i].y - mean) * rstd * gg.y + bb.y;
+            if constexpr (OUT_BF16) {
+                reinterpret_cast<uint32_t *>(y)[(long long)row * (d >> 1) + c] = pack_bf16(o0, o1);
+            } else {
+                reinterpret_cast<float2 *>(y)[(long long)row * (d >> 1) + c] = make_float2(o0, o1);
+            }
+        }
+}
+
+}  // namespace
+
+int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,
+                     cudaStream_t s) {
+    if (rows <= 0) return WH_OK;
+    if (d % 64 != 0 || d < 64 || d > 64 * MAXV) return WH_EINVAL;
+    const int grid = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
+    if (y_bf16)
+        k_layernorm<true><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+    else
+        k_layernorm<false><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
+}
+
+}  // namespace wh

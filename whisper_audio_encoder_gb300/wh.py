@@ -1,0 +1,267 @@
+"""Python binding of libwh.so (include/wh.h): argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; torch supplies device memory
+and streams.  There is no fallback: if libwh.so has not been built, or there is no GPU,
+calls raise.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libwh.so")
+
+WH_OK, WH_EINVAL, WH_ENOSPC, WH_ECUDA, WH_ETIMEOUT, WH_EBOUNDS, WH_ENODEV = range(7)
+WH_EPI_BF16, WH_EPI_GELU_BF16, WH_EPI_RESID_F32 = range(3)
+N_CTX, N_FRAMES, N_SAMPLES = 1500, 3000, 480_000
+
+_p = ctypes.c_void_p
+
+
+class wh_config(ctypes.Structure):
+    _fields_ = [("n_mels", ctypes.c_int), ("d_model", ctypes.c_int), ("n_head", ctypes.c_int),
+                ("n_layer", ctypes.c_int), ("d_ff", ctypes.c_int)]
+
+
+class wh_layer_weights(ctypes.Structure):
+    _fields_ = [("ln1_g", _p), ("ln1_b", _p), ("wq", _p), ("wk", _p), ("wv", _p), ("bq", _p), ("bv", _p),
+                ("wo", _p), ("bo", _p), ("ln2_g", _p), ("ln2_b", _p), ("w1", _p), ("b1", _p),
+                ("w2", _p), ("b2", _p)]
+
+
+class wh_weights(ctypes.Structure):
+    _fields_ = [("conv1_w", _p), ("conv1_b", _p), ("conv2_w", _p), ("conv2_b", _p), ("pos", _p),
+                ("layers", ctypes.POINTER(wh_layer_weights)), ("lnf_g", _p), ("lnf_b", _p)]
+
+
+class wh_trace_stat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
+class WhError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = code
+        super().__init__(f"{what}: {wh_strerror(code)}" if what else wh_strerror(code))
+
+
+_lib = None
+
+
+def lib():
+    """Loads libwh.so (built in-tree by whisper_audio_encoder_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m whisper_audio_encoder_gb300.build` (needs nvcc)")
+    L = ctypes.CDLL(LIB_PATH)
+    sig = {
+        "wh_frontend_workspace": (ctypes.c_size_t, [ctypes.c_int]),
+        "wh_frontend": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _p, _p, ctypes.c_size_t, _p]),
+        "wh_encode_workspace": (ctypes.c_size_t, [ctypes.POINTER(wh_config), ctypes.c_int]),
+        "wh_encode": (ctypes.c_int, [_p, ctypes.c_int, ctypes.POINTER(wh_config), ctypes.POINTER(wh_weights),
+                                     _p, _p, ctypes.c_size_t, _p]),
+        "wh_layer_norm": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, _p, _p, _p, ctypes.c_int, _p]),
+        "wh_linear": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, _p, ctypes.c_int, _p, ctypes.c_int, _p, _p]),
+        "wh_attention": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _p, _p]),
+        "wh_status": (ctypes.c_int, [_p]),
+        "wh_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "wh_selftest_timeout": (ctypes.c_int, [ctypes.c_uint64, _p]),
+        "wh_trace_enable": (ctypes.c_int, [ctypes.c_int]),
+        "wh_trace_read": (ctypes.c_int, [ctypes.POINTER(wh_trace_stat), ctypes.c_int]),
+        "wh_launch_count": (ctypes.c_int64, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def wh_strerror(code: int) -> str:
+    return lib().wh_strerror(code).decode()
+
+
+def _check(rc, what):
+    if rc != WH_OK:
+        raise WhError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ---------------------------------------------------------------------------------------
+# Entry points (same names as the C ABI), taking torch tensors
+# ---------------------------------------------------------------------------------------
+def wh_frontend_workspace(batch: int) -> int:
+    return lib().wh_frontend_workspace(batch)
+
+
+def wh_frontend(pcm, n_mels: int, mel=None, workspace=None, stream=None):
+    """pcm: float32 CUDA tensor [batch][n] -> log-mel float32 [batch][3000][n_mels]."""
+    import torch
+    assert pcm.dtype == torch.float32 and pcm.dim() == 2 and pcm.is_contiguous()
+    batch, n = pcm.shape
+    if mel is None:
+        mel = torch.empty(batch, N_FRAMES, n_mels, dtype=torch.float32, device=pcm.device)
+    if workspace is None:
+        workspace = torch.empty(max(16, wh_frontend_workspace(batch)), dtype=torch.uint8, device=pcm.device)
+    rc = lib().wh_frontend(_ptr(pcm), n, batch, n_mels, _ptr(mel), _ptr(workspace), workspace.numel(),
+                           _stream(stream))
+    _check(rc, "wh_frontend")
+    return mel
+
+
+def wh_layer_norm(x, g, b, out_bf16=True, y=None, stream=None):
+    import torch
+    rows, d = x.shape
+    if y is None:
+        y = torch.empty(rows, d, dtype=torch.bfloat16 if out_bf16 else torch.float32, device=x.device)
+    _check(lib().wh_layer_norm(_ptr(x), rows, d, _ptr(g), _ptr(b), _ptr(y), int(out_bf16), _stream(stream)),
+           "wh_layer_norm")
+    return y
+
+
+def wh_linear(a, w, bias=None, epilogue=WH_EPI_BF16, y=None, stream=None):
+    """a bf16 [rows][k], w bf16 [n][k] -> y (bf16, or the fp32 residual updated in place)."""
+    import torch
+    rows, k = a.shape
+    n = w.shape[0]
+    if y is None:
+        y = torch.empty(rows, n, dtype=torch.bfloat16, device=a.device)
+    _check(lib().wh_linear(_ptr(a), rows, k, _ptr(w), n, _ptr(bias), epilogue, _ptr(y), _stream(stream)),
+           "wh_linear")
+    return y
+
+
+def wh_attention(qkv, batch, n_ctx, n_head, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty(batch * n_ctx, n_head * 64, dtype=torch.bfloat16, device=qkv.device)
+    _check(lib().wh_attention(_ptr(qkv), batch, n_ctx, n_head, _ptr(out), _stream(stream)), "wh_attention")
+    return out
+
+
+def wh_status(stream=None) -> int:
+    return lib().wh_status(_stream(stream))
+
+
+def wh_selftest_timeout(limit_ns: int, stream=None):
+    _check(lib().wh_selftest_timeout(limit_ns, _stream(stream)), "wh_selftest_timeout")
+
+
+def wh_launch_count() -> int:
+    return lib().wh_launch_count()
+
+
+def wh_trace_enable(on: bool):
+    lib().wh_trace_enable(int(on))
+
+
+def wh_trace_read():
+    arr = (wh_trace_stat * 16)()
+    n = lib().wh_trace_read(arr, 16)
+    if n < 0:
+        raise WhError(-n, "wh_trace_read")
+    return {arr[i].name.decode(): {"launches": arr[i].launches, "total_ms": arr[i].total_ms,
+                                   "flops": arr[i].flops, "bytes": arr[i].bytes} for i in range(n)}
+
+
+# ---------------------------------------------------------------------------------------
+# Encoder: device weights + the wh_weights struct + workspace
+# ---------------------------------------------------------------------------------------
+class Encoder:
+    """Holds an encoder's weights on the device and calls wh_encode.
+
+    `weights` is a dict of numpy arrays (matrices already bf16-representable float32,
+    vectors float32), as produced by whisper_audio_encoder_gb300.synth.weights."""
+
+    def __init__(self, cfg, weights: dict, device="cuda"):
+        import torch
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self._keep = []
+
+        def mat(a):
+            t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).to(self.device)
+            self._keep.append(t)
+            return t.data_ptr()
+
+        def vec(a):
+            t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(self.device)
+            self._keep.append(t)
+            return t.data_ptr()
+
+        n_layer = len(weights["layers"])
+        self.c_cfg = wh_config(cfg.n_mels, cfg.d_model, cfg.n_head, n_layer, cfg.d_ff)
+        self._layers = (wh_layer_weights * max(1, n_layer))()
+        for i, lw in enumerate(weights["layers"]):
+            L = self._layers[i]
+            L.ln1_g, L.ln1_b = vec(lw["ln1_g"]), vec(lw["ln1_b"])
+            L.wq, L.wk, L.wv = mat(lw["wq"]), mat(lw["wk"]), mat(lw["wv"])
+            L.bq, L.bv = vec(lw["bq"]), vec(lw["bv"])
+            L.wo, L.bo = mat(lw["wo"]), vec(lw["bo"])
+            L.ln2_g, L.ln2_b = vec(lw["ln2_g"]), vec(lw["ln2_b"])
+            L.w1, L.b1 = mat(lw["w1"]), vec(lw["b1"])
+            L.w2, L.b2 = mat(lw["w2"]), vec(lw["b2"])
+        self.c_w = wh_weights(mat(weights["conv1_w"]), vec(weights["conv1_b"]), mat(weights["conv2_w"]),
+                              vec(weights["conv2_b"]), vec(weights["pos"]),
+                              ctypes.cast(self._layers, ctypes.POINTER(wh_layer_weights)),
+                              vec(weights["lnf_g"]), vec(weights["lnf_b"]))
+        self._ws = None
+        self._fe_ws = None
+
+    def workspace_bytes(self, batch: int) -> int:
+        return lib().wh_encode_workspace(ctypes.byref(self.c_cfg), batch)
+
+    def workspace(self, batch: int):
+        import torch
+        need = self.workspace_bytes(batch)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = None
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def wh_encode(self, mel, out=None, stream=None):
+        """mel float32 [batch][3000][n_mels] (device) -> float32 [batch][1500][d_model]."""
+        import torch
+        batch = mel.shape[0]
+        if out is None:
+            out = torch.empty(batch, N_CTX, self.cfg.d_model, dtype=torch.float32, device=self.device)
+        ws = self.workspace(batch)
+        rc = lib().wh_encode(_ptr(mel), batch, ctypes.byref(self.c_cfg), ctypes.byref(self.c_w), _ptr(out),
+                             _ptr(ws), ws.numel(), _stream(stream))
+        _check(rc, "wh_encode")
+        return out
+
+    def frontend_workspace(self, batch: int):
+        import torch
+        need = max(16, wh_frontend_workspace(batch))
+        if self._fe_ws is None or self._fe_ws.numel() < need:
+            self._fe_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._fe_ws
+
+    def forward(self, pcm, mel=None, out=None, stream=None):
+        """16 kHz PCM float32 [batch][n] on the device -> encoder memory [batch][1500][d]."""
+        mel = wh_frontend(pcm, self.cfg.n_mels, mel=mel, workspace=self.frontend_workspace(pcm.shape[0]),
+                          stream=stream)
+        return self.wh_encode(mel, out=out, stream=stream)
+
+    def encode_from_host(self, pcm_host, out_host, pcm_dev, mel, out_dev, stream=None):
+        """End to end from pinned host memory: copy PCM in, front end + encoder, copy the
+        memory out (all on one stream)."""
+        pcm_dev.copy_(pcm_host, non_blocking=True)
+        self.forward(pcm_dev, mel=mel, out=out_dev, stream=stream)
+        out_host.copy_(out_dev, non_blocking=True)
+        return out_host
