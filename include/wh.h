@@ -94,6 +94,25 @@ int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel,
                 void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
+ * wh_frontend_static: wh_frontend for callers that cannot allocate device memory.
+ * (The pages have no counterpart: this is an interface choice of this library.)
+ * Some callers cannot hand the library a scratch buffer at the point they call in: a
+ * real-time audio callback must not block on the CUDA allocator, and a process that gave
+ * all of its device memory to another allocator up front has none left.  This variant keeps
+ * the per-window maxima in a fixed array inside the library (WH_FRONTEND_STATIC_MAX_BATCH
+ * words, held on every GPU that loads the library until the process exits) and allocates
+ * nothing; pcm and mel are as for wh_frontend.
+ *   - batch > WH_FRONTEND_STATIC_MAX_BATCH returns WH_ENOSPC (nothing is launched).
+ *   - The first call on each device sets up the library's tables and looks up the array's
+ *     device address; make that first call before any stream capture.
+ *   - All calls on a device share the array: calls that overlap on the GPU (for example on
+ *     two streams at once) race on it.  Each call clears the maxima before using them.
+ * Errors: as wh_frontend, plus WH_ENOSPC for an oversized batch.
+ * ------------------------------------------------------------------------------------ */
+#define WH_FRONTEND_STATIC_MAX_BATCH 4096
+int wh_frontend_static(const float *pcm, int64_t n, int batch, int n_mels, float *mel, void *stream);
+
+/* ---------------------------------------------------------------------------------------
  * Encoder.  "whisper 0.9.0 API", model.nu: conv1 (k=3, s=1, pad=1) n_mels -> d, GELU;
  * conv2 (k=3, s=2, pad=1) d -> d, GELU, 3000 -> 1500 frames; + stored positions; n_layer
  * pre-LN blocks with NON-causal self-attention (scores q.k / sqrt(64), kernels.nu); final

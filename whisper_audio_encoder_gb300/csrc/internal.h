@@ -43,6 +43,9 @@ int stem_im2col_launch(const float *mel, int batch, int n_mels, void *a1, cudaSt
 int pack_conv_weight_launch(const void *w, int c_out, int c_in, void *wp, cudaStream_t s);
 int selftest_timeout_launch(const DevCtl &ctl, cudaStream_t s);
 
+// ---- per-device set-up (wh_api.cu): constant tables and status word, once per device ----
+int device_setup();
+
 // ---- tracing (wh_api.cu) ------------------------------------------------------------------
 // Kernel classes for the per-kernel timing.
 enum TraceClass { TR_FRONTEND = 0, TR_STEM_PREP, TR_GEMM, TR_ATTN, TR_LAYERNORM, TR_NCLASS };

@@ -61,6 +61,7 @@ def lib():
     sig = {
         "wh_frontend_workspace": (ctypes.c_size_t, [ctypes.c_int]),
         "wh_frontend": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _p, _p, ctypes.c_size_t, _p]),
+        "wh_frontend_static": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _p, _p]),
         "wh_encode_workspace": (ctypes.c_size_t, [ctypes.POINTER(wh_config), ctypes.c_int]),
         "wh_encode": (ctypes.c_int, [_p, ctypes.c_int, ctypes.POINTER(wh_config), ctypes.POINTER(wh_weights),
                                      _p, _p, ctypes.c_size_t, _p]),
