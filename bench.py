@@ -49,6 +49,21 @@ def _dist():
     return ws, rank, local
 
 
+def rank_windows(batch_per_gpu, rank):
+    """Window indices encoded by `rank`: each replica takes its own contiguous block."""
+    return range(rank * batch_per_gpu, (rank + 1) * batch_per_gpu)
+
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings (the slowest replica sets the step time)."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -176,13 +191,29 @@ class Clocks:
                 "samples": len(sm)}
 
 
+KERNEL_SOURCES = {"gemm_fc1": ["gemm_tc.cu", "common.cuh"], "attention": ["attention.cu", "common.cuh"]}
+
+
+def _sources_hash(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "whisper_audio_encoder_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def _traffic_from_profiles(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary (or None)."""
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu summary, or None
+    when there is none or the kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
     with open(path) as fh:
-        return json.load(fh).get(kernel)
+        rec = json.load(fh).get(kernel)
+    if not rec or rec.get("sources_sha256") != _sources_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return rec["dram_bytes_per_launch"]
 
 
 def run_ours(args):
@@ -204,7 +235,7 @@ def run_ours(args):
     weights = synth.weights(cfg)
     enc = wh.Encoder(cfg, weights, device=f"cuda:{local}")
     del weights
-    pcm_np = synth.waveforms(cfg, windows=range(rank * B, rank * B + B))
+    pcm_np = synth.waveforms(cfg, windows=rank_windows(B, rank))
     pcm_h = torch.from_numpy(pcm_np).pin_memory()
     pcm_d = pcm_h.cuda()
     mel_d = torch.empty(B, 3000, cfg.n_mels, device="cuda")
@@ -258,9 +289,8 @@ def run_ours(args):
         e2e_ms = e0.elapsed_time(e1) / args.steps
 
     if dist is not None:
-        t = torch.tensor([ms, e2e_ms or 0.0], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), (float(t[1]) if e2e_ms is not None else None)
+        ms, e2e_max = max_over_ranks([ms, e2e_ms or 0.0], dist, device="cuda")
+        e2e_ms = e2e_max if e2e_ms is not None else None
     st = wh.wh_status()
     if st != wh.WH_OK:
         raise RuntimeError(f"device status after the timed region: {wh.wh_strerror(st)}")
@@ -271,12 +301,15 @@ def run_ours(args):
     peaks = _peaks()
     value = B * ws * 1000.0 / ms
     flops_window = cfg.flops_per_window()["total"]
-    g = stats.get("gemm", {"launches": 0, "total_ms": 0.0, "flops": 0.0})
+    g = stats.get("gemm_fc1", {"launches": 0, "total_ms": 0.0, "flops": 0.0})
     gemm_avg_ms = g["total_ms"] / max(1, g["launches"])
     gemm_flops_launch = g["flops"] / max(1, g["launches"])
     achieved = gemm_flops_launch / (gemm_avg_ms * 1e-3) / 1e12 if gemm_avg_ms > 0 else 0.0
     peak = peaks["bf16_tflops_sustained"]
-    traffic = _traffic_from_profiles("gemm")
+    traffic = _traffic_from_profiles("gemm_fc1")
+    gemm_all = [v for k, v in stats.items() if k.startswith("gemm")]
+    gemm_ms = sum(v["total_ms"] for v in gemm_all)
+    gemm_tflops = sum(v["flops"] for v in gemm_all) / max(1e-12, gemm_ms * 1e-3) / 1e12
     kernels = {k: {"launches": v["launches"], "ms_per_step": v["total_ms"] / args.steps,
                    "share": v["total_ms"] / max(1e-9, sum(s["total_ms"] for s in stats.values())),
                    **({"tflops": v["flops"] / (v["total_ms"] * 1e-3) / 1e12} if v["flops"] > 0 else {}),
@@ -289,9 +322,11 @@ def run_ours(args):
         "config": _workload(cfg, ws),
         "encoder_tflops": flops_window * B * ws / (ms * 1e-3) / 1e12,
         "frac_of_bf16_peak": flops_window * B / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
-        "roofline": {"bound": "tensor", "kernel": "gemm (tcgen05, all encoder dense layers)",
+        "roofline": {"bound": "tensor", "kernel": "k_gemm fc1 (tcgen05; M = B*1500, N = 4d, K = d, GELU epilogue)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": f"{peaks['source']} bf16 sustained", "traffic": traffic},
+                     "peak_source": f"{peaks['source']} bf16 sustained", "traffic": traffic,
+                     "flops_per_launch": gemm_flops_launch, "ms_per_launch": gemm_avg_ms},
+        "gemm_all_tflops": gemm_tflops,
         "kernels": kernels,
         "gpu_launches": int(launches),
         "clocks": clk,

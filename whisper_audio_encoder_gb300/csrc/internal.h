@@ -48,7 +48,10 @@ int device_setup();
 
 // ---- tracing (wh_api.cu) ------------------------------------------------------------------
 // Kernel classes for the per-kernel timing.
-enum TraceClass { TR_FRONTEND = 0, TR_STEM_PREP, TR_GEMM, TR_ATTN, TR_LAYERNORM, TR_NCLASS };
+enum TraceClass {
+    TR_FRONTEND = 0, TR_STEM_PREP, TR_GEMM, TR_ATTN, TR_LAYERNORM,
+    TR_GEMM_CONV, TR_GEMM_QKV, TR_GEMM_OUT, TR_GEMM_FC1, TR_GEMM_FC2, TR_NCLASS
+};
 void trace_begin(int cls, cudaStream_t s);
 void trace_end(int cls, cudaStream_t s, double flops, double bytes);
 void count_launch(int n = 1);

@@ -79,7 +79,8 @@ struct TraceRec {
     cudaEvent_t e0, e1;
     double flops, bytes;
 };
-const char *const kTraceNames[TR_NCLASS] = {"frontend", "stem_prep", "gemm", "attention", "layernorm"};
+const char *const kTraceNames[TR_NCLASS] = {"frontend", "stem_prep", "gemm", "attention", "layernorm",
+                                             "gemm_conv", "gemm_qkv", "gemm_out", "gemm_fc1", "gemm_fc2"};
 std::mutex g_tr_mu;
 bool g_tr_on = false;
 std::vector<TraceRec> g_tr;
@@ -147,10 +148,10 @@ int check_weights(const wh_config *c, const wh_weights *w) {
     return WH_OK;
 }
 
-int run_gemm(const GemmDesc &g, int mode, const DevState *st, cudaStream_t s) {
-    trace_begin(TR_GEMM, s);
+int run_gemm(const GemmDesc &g, int mode, const DevState *st, cudaStream_t s, int cls = TR_GEMM) {
+    trace_begin(cls, s);
     const int rc = gemm_launch(g, mode, ctl_of(st), st->num_sms, s);
-    trace_end(TR_GEMM, s, 2.0 * g.M * (double)g.N * g.K,
+    trace_end(cls, s, 2.0 * g.M * (double)g.N * g.K,
               2.0 * ((double)g.M * g.K + (double)g.N * g.K) +
                   (double)g.M * g.N * (mode == GEMM_RESID_F32 ? 8.0 : (mode == GEMM_CONV2 ? 4.0 : 2.0)));
     return rc;
@@ -277,13 +278,13 @@ int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weight
     {
         GemmDesc g = gemm(a1, 3 * M, batch * N_FRAMES, 3 * M, w1p, 3 * M, d, w->conv1_b, qkv, 3LL * d);
         g.rows_per_win = N_FRAMES;
-        if ((rc = run_gemm(g, GEMM_CONV1, st, s))) return rc;
+        if ((rc = run_gemm(g, GEMM_CONV1, st, s, TR_GEMM_CONV))) return rc;
     }
     {
         GemmDesc g = gemm(qkv, 3 * d, rows, 3 * d, w2p, 3 * d, d, w->conv2_b, x, d);
         g.pos = w->pos;
         g.rows_per_win = N_CTX;
-        if ((rc = run_gemm(g, GEMM_CONV2, st, s))) return rc;
+        if ((rc = run_gemm(g, GEMM_CONV2, st, s, TR_GEMM_CONV))) return rc;
     }
     // ---- blocks
     for (int l = 0; l < cfg->n_layer; ++l) {
@@ -298,17 +299,20 @@ int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weight
             g.seg_n = d;
             g.bias[1] = nullptr;  // k_proj has no bias
             g.bias[2] = Lw.bv;
-            if ((rc = run_gemm(g, GEMM_BF16, st, s))) return rc;
+            if ((rc = run_gemm(g, GEMM_BF16, st, s, TR_GEMM_QKV))) return rc;
         }
         trace_begin(TR_ATTN, s);
         if ((rc = attention_launch(qkv, batch, N_CTX, H, ao, s))) return rc;
         trace_end(TR_ATTN, s, 4.0 * batch * (double)N_CTX * N_CTX * d, (double)rows * d * 8.0);
-        if ((rc = run_gemm(gemm(ao, d, rows, d, Lw.wo, d, d, Lw.bo, x, d), GEMM_RESID_F32, st, s))) return rc;
+        if ((rc = run_gemm(gemm(ao, d, rows, d, Lw.wo, d, d, Lw.bo, x, d), GEMM_RESID_F32, st, s, TR_GEMM_OUT)))
+            return rc;
         trace_begin(TR_LAYERNORM, s);
         if ((rc = layernorm_launch(x, rows, d, Lw.ln2_g, Lw.ln2_b, xn, 1, s))) return rc;
         trace_end(TR_LAYERNORM, s, 0.0, (double)rows * d * 6.0);
-        if ((rc = run_gemm(gemm(xn, d, rows, d, Lw.w1, d, f, Lw.b1, hb, f), GEMM_GELU_BF16, st, s))) return rc;
-        if ((rc = run_gemm(gemm(hb, f, rows, f, Lw.w2, f, d, Lw.b2, x, d), GEMM_RESID_F32, st, s))) return rc;
+        if ((rc = run_gemm(gemm(xn, d, rows, d, Lw.w1, d, f, Lw.b1, hb, f), GEMM_GELU_BF16, st, s, TR_GEMM_FC1)))
+            return rc;
+        if ((rc = run_gemm(gemm(hb, f, rows, f, Lw.w2, f, d, Lw.b2, x, d), GEMM_RESID_F32, st, s, TR_GEMM_FC2)))
+            return rc;
     }
     trace_begin(TR_LAYERNORM, s);
     rc = layernorm_launch(x, rows, d, w->lnf_g, w->lnf_b, out, 0, s);
