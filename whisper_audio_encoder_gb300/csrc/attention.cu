@@ -1,14 +1,26 @@
-// Non-causal multi-head self-attention, head_dim 64 ("whisper 0.9.0 API", kernels.nu:
-// attn_f "fused attention, online softmax (hd = 64)", attn_sc "scores = q.k / sqrt(hd), NO
-// causal mask", attn_out "softmax(scores) . v"; "How Audio Becomes Words", section "The
-// Encoder: Understand Once": the full 1500 x 1500 square, no mask, no RoPE).
+// Non-causal multi-head self-attention, head_dim 64, on the 5th-generation tensor cores
+// ("whisper 0.9.0 API", kernels.nu: attn_f "fused attention, online softmax (hd = 64)",
+// attn_sc "scores = q.k / sqrt(hd), NO causal mask", attn_out "softmax(scores) . v";
+// "How Audio Becomes Words", section "The Encoder: Understand Once": the full 1500 x 1500
+// square, no mask, no RoPE).
 //
-// Flash-style: one block = 64 queries of one (window, head), 4 warps x 16 query rows.
-// K/V tiles of 64 keys stream through a double-buffered shared-memory ring (cp.async,
-// XOR-swizzled 16-byte chunks); S = Q K^T and O += P V on bf16 tensor-core MMAs with fp32
-// accumulation; the softmax is online in registers (running max and sum per row, base-2
-// exponent with the 1/8 * log2(e) scale folded in).  Keys past n_ctx (the 1500 = 23 * 64 + 28
-// tail) are masked with -inf; the score matrix never reaches memory.
+// One CTA = two 128-query tiles (t = 0, 1) of one (window, head); keys stream through in
+// tiles of 128.  q/k/v are read straight from the QKV projection's output [rows][3 D] by TMA
+// (128-byte swizzle).  Per key tile j and query tile t:
+//   S_t = Q_t K_j^T            tcgen05.mma M=128 N=128 K=64 into TMEM (128 fp32 columns)
+//   softmax warps (4 per tile, one query row per thread) read S_t from TMEM, keep the running
+//   row maximum m and sum l, write P = exp2((S - m) / 8 * log2 e) as bf16 into shared memory
+//   (K-major, 128-byte swizzle)
+//   O_t += P_t V_j             tcgen05.mma M=128 N=64 K=128 into TMEM (V read MN-major)
+//   O_t accumulates in TMEM across key tiles; it is rescaled (by the softmax warps) only when
+//   the running maximum grows by more than 2^8 in the exp2 domain
+// The MMA warp alternates the two query tiles so that one tile's softmax overlaps the other
+// tile's MMAs.  Keys at or past n_ctx (the last tile: 1500 = 11 * 128 + 92) are masked; the
+// score matrix never leaves the SM.
+//
+// Roles: warp 0 TMA producer, warp 1 TMEM allocation + MMA issuer (warps 2-3 idle), warps
+// 4-7 softmax of tile 0, warps 8-11 softmax of tile 1 (warp w reads TMEM lanes 32 (w % 4) ..).  Every wait is bounded (DevCtl::wait_ns): on expiry
+// the block records WH_ETIMEOUT, winds down, drains its own copies and MMAs, frees TMEM.
 #include "common.cuh"
 #include "internal.h"
 
@@ -16,183 +28,326 @@ namespace wh {
 
 namespace {
 
-constexpr int BQ = 64, BKV = 64, ATT_THREADS = 128;
+constexpr int QT = 128, KT = 128, HD = 64, NST = 3;
+constexpr int THREADS = 384;
+// Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512); the producer /
+// MMA warpgroup drops to 88 and the two softmax warpgroups rise to 208:
+// 128 x 88 + 256 x 208 = 64512, exactly the launch total.
+constexpr int REG_LOW = 88, REG_HIGH = 208;
+static_assert(128 * REG_LOW + 256 * REG_HIGH <= THREADS * 168, "register split exceeds the launch total");
+constexpr int Q_BYTES = QT * HD * 2;     // 16 KB
+constexpr int KV_BYTES = KT * HD * 2;    // 16 KB
+constexpr int P_BYTES = QT * KT * 2;     // 32 KB: two K-slabs of 64 keys
+constexpr int OFF_Q = 0;
+constexpr int OFF_KV = 2 * Q_BYTES;
+constexpr int OFF_P = OFF_KV + NST * 2 * KV_BYTES;
+constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+struct AttnArgs {
+    int n_ctx, n_head, nkv;
+    __nv_bfloat16 *out;
+    float scale_log2;
+    DevCtl ctl;
+};
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// Byte offset of 16-byte chunk `ch` of row `r` in a [64][64] bf16 tile (128-byte rows).
-__device__ __forceinline__ uint32_t toff(int r, int ch) { return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4)); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// MN-major operand (V: rows = keys (the K dimension), 64 contiguous head dims = one 128-byte
+// swizzle atom along N): 8-row K groups 1024 bytes apart.  Only one atom along N, so the
+// leading offset is never used; it is set to the same 1024 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(1024 >> 4) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
 
-__global__ void __launch_bounds__(ATT_THREADS) k_attention(const __nv_bfloat16 *__restrict__ qkv, int n_ctx,
-                                                           int n_head, __nv_bfloat16 *__restrict__ out,
-                                                           float scale_log2) {
-    __shared__ __align__(128) uint8_t sQ[BQ * 128];
-    __shared__ __align__(128) uint8_t sK[2][BKV * 128];
-    __shared__ __align__(128) uint8_t sV[2][BKV * 128];
+__global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_constant__ CUtensorMap tm, const AttnArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *sQ = smem + OFF_Q;
+    uint8_t *sKV = smem + OFF_KV;      // stage s: K at s * 32 KB, V at s * 32 KB + 16 KB
+    uint8_t *sP = smem + OFF_P;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint64_t *q_full = bars;
+    uint64_t *kv_full = bars + 1;
+    uint64_t *kv_empty = kv_full + NST;
+    uint64_t *s_full = kv_empty + NST;
+    uint64_t *s_free = s_full + 2;
+    uint64_t *p_full = s_free + 2;
+    uint64_t *o_full = p_full + 2;
+    uint64_t *drain = o_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, b = blockIdx.z;
-    const int D = n_head * 64;
-    const long long ld = 3LL * D;
-    const __nv_bfloat16 *base = qkv + (long long)b * n_ctx * ld;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q0 = blockIdx.x * BQ;
+    const int D = p.n_head * HD;
+    const int q0 = blockIdx.x * 2 * QT;
+    const int row0 = b * p.n_ctx;
 
-    for (int c = tid; c < BQ * 8; c += ATT_THREADS) {
-        const int r = c >> 3, ch = c & 7, qr = q0 + r;
-        const __nv_bfloat16 *src = base + (long long)min(qr, n_ctx - 1) * ld + h * 64 + ch * 8;
-        cp_async16(smem_u32(sQ) + toff(r, ch), src, qr < n_ctx ? 16 : 0);
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(kv_full + s, 1);
+            mbar_init(kv_empty + s, 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(s_full + t, 1);
+            mbar_init(s_free + t, 4);
+            mbar_init(p_full + t, 4);
+            mbar_init(o_full + t, 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm);
     }
-    auto load_kv = [&](int j, int buf) {
-        const int k0 = j * BKV;
-        for (int c = tid; c < BKV * 8; c += ATT_THREADS) {
-            const int r = c >> 3, ch = c & 7, kr = k0 + r;
-            const long long roff = (long long)min(kr, n_ctx - 1) * ld + h * 64 + ch * 8;
-            const int bytes = kr < n_ctx ? 16 : 0;
-            cp_async16(smem_u32(sK[buf]) + toff(r, ch), base + roff + D, bytes);
-            cp_async16(smem_u32(sV[buf]) + toff(r, ch), base + roff + 2 * D, bytes);
-        }
-    };
-    load_kv(0, 0);
-    cp_async_commit();
-
-    const int nkv = (n_ctx + BKV - 1) / BKV;
-    float o[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    uint32_t qf[4][4];
-    const int mi = lane >> 3, r8 = lane & 7;
-
-    for (int j = 0; j < nkv; ++j) {
-        const int buf = j & 1;
-        if (j + 1 < nkv) load_kv(j + 1, buf ^ 1);
-        cp_async_commit();
-        cp_async_wait1();
-        __syncthreads();
-        if (j == 0) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                ldsm_x4(smem_u32(sQ) + toff(warp * 16 + (mi & 1) * 8 + r8, kk * 2 + (mi >> 1)), qf[kk][0], qf[kk][1],
-                        qf[kk][2], qf[kk][3]);
-        }
-        float s[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.0f;
-        const uint32_t kbase = smem_u32(sK[buf]);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kbase + toff((2 * np + (mi >> 1)) * 8 + r8, kk * 2 + (mi & 1)), b0, b1, b2, b3);
-                mma16816(s[2 * np], qf[kk], b0, b1);
-                mma16816(s[2 * np + 1], qf[kk], b2, b3);
-            }
-        const bool tail = (j + 1) * BKV > n_ctx;
-        float mx0 = m0, mx1 = m1;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float v = s[nt][e] * scale_log2;
-                if (tail && j * BKV + nt * 8 + (lane & 3) * 2 + (e & 1) >= n_ctx) v = -INFINITY;
-                s[nt][e] = v;
-            }
-            mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-            mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-        }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float a0 = ex2(m0 - mx0), a1 = ex2(m1 - mx1);
-        m0 = mx0;
-        m1 = mx1;
-        float rs0 = 0.0f, rs1 = 0.0f;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            s[nt][0] = ex2(s[nt][0] - m0);
-            s[nt][1] = ex2(s[nt][1] - m0);
-            s[nt][2] = ex2(s[nt][2] - m1);
-            s[nt][3] = ex2(s[nt][3] - m1);
-            rs0 += s[nt][0] + s[nt][1];
-            rs1 += s[nt][2] + s[nt][3];
-            o[nt][0] *= a0;
-            o[nt][1] *= a0;
-            o[nt][2] *= a1;
-            o[nt][3] *= a1;
-        }
-        l0 = l0 * a0 + rs0;
-        l1 = l1 * a1 + rs1;
-        uint32_t pf[4][4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            pf[kk][0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-            pf[kk][1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-            pf[kk][2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-            pf[kk][3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-        }
-        const uint32_t vbase = smem_u32(sV[buf]);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vbase + toff(kk * 16 + (mi & 1) * 8 + r8, 2 * np + (mi >> 1)), b0, b1, b2, b3);
-                mma16816(o[2 * np], pf[kk], b0, b1);
-                mma16816(o[2 * np + 1], pf[kk], b2, b3);
-            }
-        __syncthreads();
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
     }
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float i0 = 1.0f / l0, i1 = 1.0f / l1;
-    const int r0 = q0 + warp * 16 + (lane >> 2), r1 = r0 + 8;
-    uint32_t *o0 = reinterpret_cast<uint32_t *>(out + ((long long)b * n_ctx + r0) * D + h * 64);
-    uint32_t *o1 = reinterpret_cast<uint32_t *>(out + ((long long)b * n_ctx + r1) * D + h * 64);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_LOW));
+      if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        uint32_t issued = 0, last_parity = 0;
+        mbar_arrive_expect_tx(q_full, 2 * Q_BYTES);
+        tma_load_2d(sQ, &tm, q_full, h * HD, row0 + q0);
+        tma_load_2d(sQ + Q_BYTES, &tm, q_full, h * HD, row0 + q0 + QT);
+        for (int j = 0; j < p.nkv; ++j) {
+            const int s = j % NST;
+            const uint32_t ph = (uint32_t)(j / NST) & 1u;
+            if (*abort_flag || !mbar_wait(kv_empty + s, ph ^ 1u, p.ctl)) {
+                *abort_flag = 1;
+                break;
+            }
+            uint8_t *k = sKV + s * 2 * KV_BYTES;
+            mbar_arrive_expect_tx(kv_full + s, 2 * KV_BYTES);
+            tma_load_2d(k, &tm, kv_full + s, D + h * HD, row0 + j * KT);
+            tma_load_2d(k + KV_BYTES, &tm, kv_full + s, 2 * D + h * HD, row0 + j * KT);
+            issued |= 1u << s;
+            last_parity = (last_parity & ~(1u << s)) | (ph << s);
+        }
+        mbar_wait(q_full, 0, p.ctl);
+        for (int s = 0; s < NST; ++s)
+            if ((issued >> s) & 1u) mbar_wait(kv_full + s, (last_parity >> s) & 1u, p.ctl);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        // Per key tile j: S_t(j+1) as soon as the softmax of tile t has read S_t(j), then
+        // O_t += P_t(j) V_j once P_t(j) is in shared memory.
+        constexpr uint32_t IDESC_S = idesc_bf16_f32(QT, KT);
+        constexpr uint32_t IDESC_O = idesc_bf16_f32(QT, HD) | (1u << 16);  // B (V) is MN-major
+        const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV), sp = smem_u32(sP);
+        bool ok = mbar_wait(q_full, 0, p.ctl) && mbar_wait(kv_full, 0, p.ctl);
+        auto issue_s = [&](int t, int s) {
+            const uint64_t a = sdesc_sw128(sq + t * Q_BYTES), bk = sdesc_sw128(skv + s * 2 * KV_BYTES);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-        const int c2 = nt * 4 + (lane & 3);  // bf16 pair index within the head
-        if (r0 < n_ctx) o0[c2] = pack_bf16(o[nt][0] * i0, o[nt][1] * i0);
-        if (r1 < n_ctx) o1[c2] = pack_bf16(o[nt][2] * i1, o[nt][3] * i1);
+            for (int k = 0; k < HD / 16; ++k)
+                umma_bf16(tmem + 128u * t, a + (uint64_t)(2 * k), bk + (uint64_t)(2 * k), IDESC_S, k != 0);
+            umma_commit(s_full + t);
+        };
+        if (ok) {
+            tc_fence_after();
+            issue_s(0, 0);
+            issue_s(1, 0);
+        }
+        for (int j = 0; ok && j < p.nkv; ++j) {
+            const int s = j % NST;
+            if (j + 1 < p.nkv) {
+                const int s1 = (j + 1) % NST;
+                ok = !*abort_flag && mbar_wait(kv_full + s1, (uint32_t)((j + 1) / NST) & 1u, p.ctl);
+                for (int t = 0; t < 2 && ok; ++t) {
+                    ok = mbar_wait(s_free + t, (uint32_t)j & 1u, p.ctl);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(t, s1);
+                }
+            }
+            for (int t = 0; t < 2 && ok; ++t) {
+                ok = !*abort_flag && mbar_wait(p_full + t, (uint32_t)j & 1u, p.ctl);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t pa = sp + t * P_BYTES, vb = skv + s * 2 * KV_BYTES + KV_BYTES;
+#pragma unroll
+                for (int k = 0; k < KT / 16; ++k)
+                    umma_bf16(tmem + 256u + 64u * t, sdesc_sw128(pa + (k >> 2) * 16384) + (uint64_t)(2 * (k & 3)),
+                              sdesc_sw128_mn(vb + k * 2048), IDESC_O, (j | k) != 0);
+                umma_commit(o_full + t);
+            }
+            if (!ok) break;
+            umma_commit(kv_empty + s);  // K/V stage s is free once the MMAs issued so far are done
+        }
+        if (!ok) *abort_flag = 1;
+        umma_commit(drain);
+        mbar_wait(drain, 0, p.ctl);
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_HIGH));
+        // ---------------- softmax: one query row per thread ----------------
+        // O accumulates in TMEM.  The row maximum m used for the exponentials is only raised
+        // (and O, l rescaled) when the true maximum exceeds it by more than 2^8 in the exp2
+        // domain, so exponentials stay <= 256 and the rescale is rare.
+        const int t = (warp - 4) >> 2;
+        const int r = (warp & 3) * 32 + lane;                 // TMEM lane quarter = warp % 4
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + 128u * t;
+        const uint32_t tO = tmem + lane_off + 256u + 64u * t;
+        uint8_t *prow = sP + t * P_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < p.nkv; ++j) {
+            ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(s_full + t, (uint32_t)j & 1u, p.ctl));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sv[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, sv[c]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free + t);           // S_t may now be overwritten
+            const int kvalid = p.n_ctx - j * KT;               // keys of this tile inside the window
+            if (kvalid < KT) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * c + i >= kvalid) sv[c][i] = 0xff800000u;  // -inf
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
+            const float m_new = fmaxf(m, mx);
+            if (j == 0) {
+                m = m_new;
+            } else {
+                // PV of the previous tile is done: O is stable and the P buffer is free.
+                ok = __all_sync(0xffffffffu, mbar_wait(o_full + t, (uint32_t)(j - 1) & 1u, p.ctl));
+                if (!ok) break;
+                tc_fence_after();
+                const bool need = (m_new - m) * sl2 > 8.0f;
+                if (__any_sync(0xffffffffu, need)) {
+                    float f = 1.0f;
+                    if (need) {
+                        f = ex2((m - m_new) * sl2);
+                        l *= f;
+                        m = m_new;
+                    }
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t v[32];
+                        tmem_ld32(tO + 32u * half, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                        tmem_st32(tO + 32u * half, v);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            const float mc = m * sl2;
+            float rs = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float e = ex2(fmaf(__uint_as_float(sv[c][i]), sl2, -mc));
+                    rs += e;
+                    sv[c][i] = __float_as_uint(e);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = c * 4 + q;               // 16-byte chunk of the 256-byte row
+                    uint8_t *dst = prow + (chunk >> 3) * 16384 + (((chunk & 7) ^ (r & 7)) << 4);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        w[k] = pack_bf16(__uint_as_float(sv[c][8 * q + 2 * k]), __uint_as_float(sv[c][8 * q + 2 * k + 1]));
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            l += rs;
+            tc_fence_before();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full + t);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full + t, (uint32_t)(p.nkv - 1) & 1u, p.ctl));
+        if (!ok) {
+            *abort_flag = 1;
+        } else {
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            const int q = q0 + t * QT + r;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[32];
+                tmem_ld32(tO + 32u * half, v);
+                tmem_wait_ld();
+                if (q < p.n_ctx) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((long long)row0 + q) * D + h * HD + 32 * half);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            w[k] = pack_bf16(__uint_as_float(v[8 * c + 2 * k]) * inv,
+                                             __uint_as_float(v[8 * c + 2 * k + 1]) * inv);
+                        dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
 }  // namespace
 
-int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, cudaStream_t s) {
+int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
+                     cudaStream_t s) {
     if (batch <= 0) return WH_OK;
-    dim3 grid((n_ctx + BQ - 1) / BQ, n_head, batch);
-    const float scale_log2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
-    k_attention<<<grid, ATT_THREADS, 0, s>>>(reinterpret_cast<const __nv_bfloat16 *>(qkv), n_ctx, n_head,
-                                             reinterpret_cast<__nv_bfloat16 *>(out), scale_log2);
+    const int D = n_head * HD;
+    CUtensorMap tm;
+    if (int rc = make_tmap_bf16(&tm, qkv, (long long)batch * n_ctx, 3 * D, 3 * D, 128)) return rc;
+    AttnArgs a;
+    a.n_ctx = n_ctx;
+    a.n_head = n_head;
+    a.nkv = (n_ctx + KT - 1) / KT;
+    a.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    a.scale_log2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
+    a.ctl = ctl;
+    if (cudaFuncSetAttribute(k_attention_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+        return WH_ECUDA;
+    dim3 grid((n_ctx + 2 * QT - 1) / (2 * QT), n_head, batch);
+    k_attention_tc<<<grid, THREADS, SMEM_BYTES, s>>>(tm, a);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
 }

@@ -283,33 +283,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-int encode_fn() {
-    if (g_encode) return WH_OK;
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return WH_ECUDA;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    return WH_OK;
-}
-
-// 2-D bf16 tensor map over rows x cols (row stride ld elements), box 64 x box_rows,
-// 128-byte swizzle, zero fill outside the tensor.
-int make_map(CUtensorMap *m, const void *ptr, long long rows, int cols, int ld, int box_rows) {
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-    cuuint32_t es[2] = {1u, 1u};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? WH_OK : WH_EINVAL;
-}
-
 template <int BN, int MODE>
 int launch_t(const CUtensorMap &ta, const TmapB &tb, const GemmArgs &a, int grid, cudaStream_t s) {
     auto kern = k_gemm<BN, MODE>;
@@ -334,19 +307,48 @@ int launch_mode(int mode, const CUtensorMap &ta, const TmapB &tb, const GemmArgs
 
 }  // namespace
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+}  // namespace
+
+int tmap_encoder_ready() {
+    if (g_encode) return WH_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return WH_ECUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return WH_OK;
+}
+
+// 2-D bf16 tensor map over rows x cols (row stride ld elements), box 64 x box_rows,
+// 128-byte swizzle, zero fill outside the tensor.
+int make_tmap_bf16(CUtensorMap *m, const void *ptr, long long rows, int cols, int ld, int box_rows) {
+    if (int rc = tmap_encoder_ready()) return rc;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? WH_OK : WH_EINVAL;
+}
+
 int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cudaStream_t s) {
     if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.seg_n <= 0 || g.N % g.seg_n != 0 || g.N / g.seg_n > 3 ||
         g.seg_n % 128 != 0 || g.K % 8 != 0 || g.lda % 8 != 0 || g.ldb % 8 != 0)
         return WH_EINVAL;
-    if (int rc = encode_fn()) return rc;
     const int BN = (g.seg_n % 256 == 0) ? 256 : 128;
     const int nseg = g.N / g.seg_n;
     CUtensorMap ta;
     TmapB tb;
-    if (int rc = make_map(&ta, g.a, g.M, g.K, g.lda, BM)) return rc;
+    if (int rc = make_tmap_bf16(&ta, g.a, g.M, g.K, g.lda, BM)) return rc;
     for (int i = 0; i < 3; ++i) {
         const void *b = g.b[i < nseg ? i : 0];
-        if (int rc = make_map(&tb.m[i], b, g.seg_n, g.K, g.ldb, BN)) return rc;
+        if (int rc = make_tmap_bf16(&tb.m[i], b, g.seg_n, g.K, g.ldb, BN)) return rc;
     }
     GemmArgs a;
     a.M = g.M;

@@ -27,6 +27,10 @@ struct GemmDesc {
     const float *pos;                     // GEMM_CONV2: [rows_per_win][N]
     int rows_per_win;                     // GEMM_CONV1: c1 frames per window; GEMM_CONV2: positions
 };
+// 2-D bf16 TMA descriptor: rows x cols (row stride ld elements), box 64 x box_rows, 128-byte
+// swizzle, zero fill outside.  Returns a WH_* code.
+int make_tmap_bf16(CUtensorMap *m, const void *ptr, long long rows, int cols, int ld, int box_rows);
+
 // Returns a WH_* code.  Encodes the tensor maps and launches the persistent tcgen05 kernel.
 int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cudaStream_t s);
 
@@ -38,7 +42,8 @@ int frontend_launch(const float *pcm, int64_t n, int batch, int n_mels, float *m
 // ---- other kernels ---------------------------------------------------------------------
 int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,
                      cudaStream_t s);
-int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, cudaStream_t s);
+int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
+                     cudaStream_t s);
 int stem_im2col_launch(const float *mel, int batch, int n_mels, void *a1, cudaStream_t s);
 int pack_conv_weight_launch(const void *w, int c_out, int c_in, void *wp, cudaStream_t s);
 int selftest_timeout_launch(const DevCtl &ctl, cudaStream_t s);
