@@ -233,11 +233,16 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
                     for (int i = 0; i < 32; ++i)
                         if (32 * c + i >= kvalid) sv[c][i] = 0xff800000u;  // -inf
             }
-            float mx = -INFINITY;
+            // row maximum: 8 independent partial maxima, then a tree (no 128-long chain)
+            float pm[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) pm[k] = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
+                for (int i = 0; i < 32; ++i) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(sv[c][i]));
+            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             const float m_new = fmaxf(m, mx);
             if (j == 0) {
                 m = m_new;
@@ -267,13 +272,15 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
                 }
             }
             const float mc = m * sl2;
-            float rs = 0.0f;
+            float ps[8];                                       // 8 independent partial sums
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ps[k] = 0.0f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float e = ex2(fmaf(__uint_as_float(sv[c][i]), sl2, -mc));
-                    rs += e;
+                    ps[i & 7] += e;
                     sv[c][i] = __float_as_uint(e);
                 }
 #pragma unroll
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
                     *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            l += rs;
+            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             tc_fence_before();
             fence_proxy_async_smem();
             __syncwarp();
