@@ -73,6 +73,19 @@ def test_linear(M, K, N, epi):
     assert wh.wh_status() == wh.WH_OK
 
 
+def test_gelu_epilogue_within_bf16_rounding_of_exact_gelu():
+    """Identity weights feed chosen values straight into the fc1 epilogue: its GELU (erf form,
+    Abramowitz-Stegun 7.1.26 inside) must round to within one bf16 step of the exact GELU."""
+    x = np.linspace(-8.0, 8.0, 256 * 128).reshape(256, 128)
+    a = bf16_round_np(x)
+    w = np.eye(128, dtype=np.float32)
+    y = wh.wh_linear(_dev(a, torch.bfloat16), _dev(w, torch.bfloat16), None, wh.WH_EPI_GELU_BF16)
+    torch.cuda.synchronize()
+    ref = R.gelu(a.astype(np.float64))
+    got = y.float().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
 def test_linear_without_bias():
     rng = np.random.default_rng(5)
     a = bf16_round_np(rng.standard_normal((200, 128)))

@@ -52,14 +52,7 @@ struct AttnArgs {
     DevCtl ctl;
 };
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
+__device__ __forceinline__ float ex2(float x) { return ex2_approx(x); }
 // MN-major operand (V: rows = keys (the K dimension), 64 contiguous head dims = one 128-byte
 // swizzle atom along N): 8-row K groups 1024 bytes apart.  Only one atom along N, so the
 // leading offset is never used; it is set to the same 1024 bytes.

@@ -24,9 +24,9 @@ namespace wh {
 
 namespace {
 
-constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int EPI_WARPS = 8;
 
 struct GemmArgs {
     int M, N, num_kb, tiles_n, num_tiles, seg_n;
@@ -40,16 +40,6 @@ struct GemmArgs {
 
 struct TmapB {
     CUtensorMap m[3];
-};
-
-template <int BN>
-struct Cfg {
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
-    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 };
 
 template <int MODE>
@@ -132,22 +122,77 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &p, int row, int c
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// CTA-pair version (cta_group::2): a cluster of two CTAs computes a 256 x BN tile.  Each
+// CTA stages its own 128 rows of A and BN/2 rows of B per k-block; the even CTA issues one
+// tcgen05.mma with M = 256 that reads the A and B halves from both CTAs' shared memory, and
+// each CTA's TMEM receives its own 128 rows of the accumulator.  Per tensor-core cycle each
+// SM now brings in 2/3 of the operand bytes of the single-CTA 128 x 256 tile.
+//   full[s]    (even CTA) TMA bytes of both CTAs + the even producer's expect_tx arrival
+//   empty[s]   (both)     the even CTA's commit, multicast to both CTAs
+//   tfull[a]   (both)     the even CTA's commit, multicast to both CTAs
+//   tempty[a]  (even CTA) 4 epilogue warps of each CTA (8 arrivals)
+// ---------------------------------------------------------------------------------------
+template <int BN>
+struct Cfg2 {
+    static constexpr int A_BYTES = 128 * BK * 2;
+    static constexpr int B_BYTES = (BN / 2) * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN == 256 ? 5 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int EPI_BUF = 8192;  // per epilogue warp: 32 rows x 64 fp32 / bf16 columns
+    static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * EPI_BUF;
+    static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+    static_assert((2 * STAGES + 5 + EPI_WARPS) * 8 + 8 <= 256, "barrier area");
+};
+
+// Bias (per output segment) and, for GELU modes, the activation, on 32 accumulator columns.
+template <int MODE>
+__device__ __forceinline__ void bias_act(const GemmArgs &p, int col, const uint32_t (&r)[32], float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    const int seg = col / p.seg_n;
+    const float *bias = seg == 0 ? p.bias0 : (seg == 1 ? p.bias1 : p.bias2);
+    if (bias != nullptr) {
+        const float4 *b4 = reinterpret_cast<const float4 *>(bias + (col - seg * p.seg_n));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 b = __ldg(b4 + j);
+            v[4 * j] += b.x;
+            v[4 * j + 1] += b.y;
+            v[4 * j + 2] += b.z;
+            v[4 * j + 3] += b.w;
+        }
+    }
+    if constexpr (MODE == GEMM_GELU_BF16) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+    }
+}
+
 template <int BN, int MODE>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TmapB tmB, const GemmArgs p) {
-    using C = Cfg<BN>;
+    k_gemm2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TmapB tmB,
+            const __grid_constant__ CUtensorMap tmOut, const GemmArgs p) {
+    using C = Cfg2<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
     uint64_t *empty = full + C::STAGES;
     uint64_t *tfull = empty + C::STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *xbar = drain + 1;  // per epilogue warp: its residual tile has landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xbar + EPI_WARPS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full + s, 1);
@@ -155,29 +200,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + a, 1);
-            mbar_init(tempty + a, 4);
+            mbar_init(tempty + a, 2 * EPI_WARPS);
         }
         mbar_init(drain, 1);
+        for (int w = 0; w < EPI_WARPS; ++w) mbar_init(xbar + w, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB.m[0]);
+        tma_prefetch_desc(&tmOut);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // barriers of both CTAs initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer ----------------
+        // ---------------- TMA producer (both CTAs) ----------------
         int stage = 0;
         uint32_t phase = 0, issued = 0, last_parity = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
             const int mb = tile / p.tiles_n, nb = tile - mb * p.tiles_n;
             const int n0 = nb * BN, seg = n0 / p.seg_n, nin = n0 - seg * p.seg_n;
             const CUtensorMap *mapB = &tmB.m[seg];
@@ -187,9 +235,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     break;
                 }
                 uint8_t *sa = smem + stage * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(full + stage, C::STAGE_BYTES);
-                tma_load_2d(sa, &tmA, full + stage, kb * BK, mb * BM);
-                tma_load_2d(sa + C::A_BYTES, mapB, full + stage, kb * BK, nin);
+                const uint32_t bar = mapa_shared(full + stage, 0);
+                if (leader) mbar_arrive_expect_tx(full + stage, 2 * C::STAGE_BYTES);
+                tma_load_2d_pair(sa, &tmA, bar, kb * BK, mb * 256 + (int)rank * 128);
+                tma_load_2d_pair(sa + C::A_BYTES, mapB, bar, kb * BK, nin + (int)rank * (BN / 2));
                 issued |= 1u << stage;
                 last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == C::STAGES) {
@@ -199,16 +248,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
         }
         if (!ok) *abort_flag = 1;
-        // No copy may still be landing in shared memory when the block exits.
-        for (int s = 0; s < C::STAGES; ++s)
-            if ((issued >> s) & 1u) mbar_wait(full + s, (last_parity >> s) & 1u, p.ctl);
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer ----------------
-        constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+        // The even CTA's full barriers count both CTAs' bytes: once they complete, no copy of
+        // either CTA is in flight.  (After a wait has run out, the teardown is >= 1 s later,
+        // long after any copy has landed.)
+        if (leader)
+            for (int s = 0; s < C::STAGES; ++s)
+                if ((issued >> s) & 1u) mbar_wait(full + s, (last_parity >> s) & 1u, p.ctl);
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ---------------- MMA issuer (even CTA) ----------------
+        constexpr uint32_t IDESC = idesc_bf16_f32(256, BN);
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
             if (*abort_flag || !mbar_wait(tempty + acc, acc_phase ^ 1u, p.ctl)) {
                 ok = false;
                 break;
@@ -225,31 +277,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const uint64_t ad = sdesc_sw128(sa), bd = sdesc_sw128(sa + C::A_BYTES);
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
-                    umma_bf16(d_tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC,
-                              (kb | k) != 0 ? 1u : 0u);
-                umma_commit(empty + stage);  // frees the stage once these MMAs have read it
+                    umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC,
+                                   (kb | k) != 0 ? 1u : 0u);
+                umma_commit_pair(empty + stage, 0x3);  // frees the stage in both CTAs
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            umma_commit(tfull + acc);  // accumulator ready for the epilogue
+            umma_commit_pair(tfull + acc, 0x3);  // accumulator ready in both CTAs
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
         }
         if (!ok) *abort_flag = 1;
-        umma_commit(drain);
-        mbar_wait(drain, 0, p.ctl);  // every MMA of this block has completed
+        umma_commit_pair(drain, 0x1);
+        mbar_wait(drain, 0, p.ctl);  // every MMA of this pair has completed
     } else if (warp >= 2) {
-        // ---------------- epilogue ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // ---------------- epilogue (both CTAs: own 128 rows) ----------------
+        // Two warps per TMEM lane quarter: warp w reads lanes 32 (w % 4) .. + 31 and one half
+        // of the accumulator's columns, 64 columns per TMEM round trip.  Dense outputs go
+        // through a per-warp 32 x 64 staging tile in shared memory (128-byte swizzle) and a
+        // TMA store; the fp32 residual tile is brought in by TMA first and updated in place.
+        constexpr bool TMA_EPI = MODE == GEMM_BF16 || MODE == GEMM_GELU_BF16 || MODE == GEMM_RESID_F32;
+        const int q = warp & 3, half = (warp - 2) >> 2, ew = warp - 2;
+        uint8_t *ebuf = smem + C::EPI_OFF + ew * C::EPI_BUF;
+        uint64_t *xb = xbar + ew;
+        uint32_t xphase = 0;
+        const uint32_t tempty_leader0 = mapa_shared(tempty, 0);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-            bool ok = !*abort_flag && mbar_wait(tfull + acc, acc_phase, p.ctl);
+        bool ok = true;
+        for (int tile = pair; tile < p.num_tiles; tile += npairs) {
+            ok = !*abort_flag && mbar_wait(tfull + acc, acc_phase, p.ctl);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 *abort_flag = 1;
@@ -257,50 +319,163 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             tc_fence_after();
             const int mb = tile / p.tiles_n, nb = tile - mb * p.tiles_n;
-            const int row = mb * BM + q * 32 + lane;
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            const int row0 = mb * 256 + (int)rank * 128 + q * 32, row = row0 + lane;
+            const int c0 = half * (BN / 2);
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tbase + (uint32_t)c, r);
+            for (int c = 0; c < BN / 2; c += 64) {
+                const int col = nb * BN + c0 + c;
+                if constexpr (TMA_EPI) {
+                    if (lane == 0) {
+                        bulk_wait_read0();  // the previous store has finished reading ebuf
+                        if constexpr (MODE == GEMM_RESID_F32) {
+                            fence_proxy_async_smem();
+                            mbar_arrive_expect_tx(xb, 2 * 4096);
+                            tma_load_2d(ebuf, &tmOut, xb, col, row0);
+                            tma_load_2d(ebuf + 4096, &tmOut, xb, col + 32, row0);
+                        }
+                    }
+                    __syncwarp();
+                }
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tbase + (uint32_t)c, r0);
+                tmem_ld32(tbase + (uint32_t)c + 32u, r1);
                 tmem_wait_ld();
-                if (row < p.M) epilogue_chunk<MODE>(p, row, nb * BN + c, r);
+                if (c + 64 >= BN / 2) {  // last TMEM read of this tile: hand the accumulator back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_leader0 + (uint32_t)(acc * 8));
+                }
+                if constexpr (TMA_EPI) {
+                    float v0[32], v1[32];
+                    bias_act<MODE>(p, col, r0, v0);
+                    bias_act<MODE>(p, col + 32, r1, v1);
+                    uint8_t *mine = ebuf + lane * 128;
+                    const int sw = lane & 7;
+                    if constexpr (MODE == GEMM_RESID_F32) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(xb, xphase, p.ctl));
+                        xphase ^= 1u;
+                        if (!ok) {
+                            *abort_flag = 1;
+                            break;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {  // 16-byte chunk j = columns 4j .. 4j+3
+                            float4 *a = reinterpret_cast<float4 *>(mine + ((j ^ sw) << 4));
+                            float4 *b = reinterpret_cast<float4 *>(mine + 4096 + ((j ^ sw) << 4));
+                            float4 xa = *a, xv = *b;
+                            xa.x += v0[4 * j]; xa.y += v0[4 * j + 1]; xa.z += v0[4 * j + 2]; xa.w += v0[4 * j + 3];
+                            xv.x += v1[4 * j]; xv.y += v1[4 * j + 1]; xv.z += v1[4 * j + 2]; xv.w += v1[4 * j + 3];
+                            *a = xa;
+                            *b = xv;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {  // 16-byte chunk j = columns 8j .. 8j+7
+                            const float *v = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+                            *reinterpret_cast<uint4 *>(mine + ((j ^ sw) << 4)) =
+                                make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                                           pack_bf16(v[6], v[7]));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (MODE == GEMM_RESID_F32) {
+                            tma_store_2d(&tmOut, ebuf, col, row0);
+                            tma_store_2d(&tmOut, ebuf + 4096, col + 32, row0);
+                        } else {
+                            tma_store_2d(&tmOut, ebuf, col, row0);
+                        }
+                        bulk_commit();
+                    }
+                } else if (row < p.M) {
+                    epilogue_chunk<MODE>(p, row, col, r0);
+                    epilogue_chunk<MODE>(p, row, col + 32, r1);
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty + acc);
+            if (!ok) break;
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) bulk_wait0();  // every store of this warp has completed
     }
+    tc_fence_before();
     __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still signal its barriers
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     }
 }
 
+
 template <int BN, int MODE>
-int launch_t(const CUtensorMap &ta, const TmapB &tb, const GemmArgs &a, int grid, cudaStream_t s) {
-    auto kern = k_gemm<BN, MODE>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM_BYTES) !=
+int launch_pair_t(const CUtensorMap &ta, const TmapB &tb, const CUtensorMap &to, const GemmArgs &a, int grid,
+                  cudaStream_t s) {
+    auto kern = k_gemm2<BN, MODE>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<BN>::SMEM_BYTES) !=
         cudaSuccess)
         return WH_ECUDA;
-    kern<<<grid, GEMM_THREADS, Cfg<BN>::SMEM_BYTES, s>>>(ta, tb, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg2<BN>::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, to, a) != cudaSuccess) return WH_ECUDA;
     return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
 }
 
+// Number of CTA pairs of k_gemm2<BN, *> that can be resident at once (cached per device).
 template <int BN>
-int launch_mode(int mode, const CUtensorMap &ta, const TmapB &tb, const GemmArgs &a, int grid, cudaStream_t s) {
+int max_active_pairs(int num_sms) {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+    if (cached[dev] > 0) return cached[dev];
+    auto kern = k_gemm2<BN, GEMM_BF16>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<BN>::SMEM_BYTES) !=
+        cudaSuccess)
+        return num_sms / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms, 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg2<BN>::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = num_sms / 2;
+    }
+    cached[dev] = n;
+    return n;
+}
+
+template <int BN>
+int launch_pair_mode(int mode, const CUtensorMap &ta, const TmapB &tb, const CUtensorMap &to, const GemmArgs &a,
+                     int grid, cudaStream_t s) {
     switch (mode) {
-        case GEMM_BF16: return launch_t<BN, GEMM_BF16>(ta, tb, a, grid, s);
-        case GEMM_GELU_BF16: return launch_t<BN, GEMM_GELU_BF16>(ta, tb, a, grid, s);
-        case GEMM_RESID_F32: return launch_t<BN, GEMM_RESID_F32>(ta, tb, a, grid, s);
-        case GEMM_CONV1: return launch_t<BN, GEMM_CONV1>(ta, tb, a, grid, s);
-        case GEMM_CONV2: return launch_t<BN, GEMM_CONV2>(ta, tb, a, grid, s);
+        case GEMM_BF16: return launch_pair_t<BN, GEMM_BF16>(ta, tb, to, a, grid, s);
+        case GEMM_GELU_BF16: return launch_pair_t<BN, GEMM_GELU_BF16>(ta, tb, to, a, grid, s);
+        case GEMM_RESID_F32: return launch_pair_t<BN, GEMM_RESID_F32>(ta, tb, to, a, grid, s);
+        case GEMM_CONV1: return launch_pair_t<BN, GEMM_CONV1>(ta, tb, to, a, grid, s);
+        case GEMM_CONV2: return launch_pair_t<BN, GEMM_CONV2>(ta, tb, to, a, grid, s);
     }
     return WH_EINVAL;
 }
@@ -323,18 +498,28 @@ int tmap_encoder_ready() {
     return WH_OK;
 }
 
+namespace {
+int make_tmap(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *ptr, long long rows, int cols, int ld,
+              int box_cols, int box_rows) {
+    if (int rc = tmap_encoder_ready()) return rc;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * esize};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = g_encode(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? WH_OK : WH_EINVAL;
+}
+}  // namespace
+
 // 2-D bf16 tensor map over rows x cols (row stride ld elements), box 64 x box_rows,
 // 128-byte swizzle, zero fill outside the tensor.
 int make_tmap_bf16(CUtensorMap *m, const void *ptr, long long rows, int cols, int ld, int box_rows) {
-    if (int rc = tmap_encoder_ready()) return rc;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-    cuuint32_t es[2] = {1u, 1u};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? WH_OK : WH_EINVAL;
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, rows, cols, ld, 64, box_rows);
+}
+int make_tmap_f32(CUtensorMap *m, const void *ptr, long long rows, int cols, int ld, int box_rows) {
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, rows, cols, ld, 32, box_rows);
 }
 
 int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cudaStream_t s) {
@@ -345,17 +530,18 @@ int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cud
     const int nseg = g.N / g.seg_n;
     CUtensorMap ta;
     TmapB tb;
-    if (int rc = make_tmap_bf16(&ta, g.a, g.M, g.K, g.lda, BM)) return rc;
+    // CTA pairs: each CTA loads 128 rows of A and BN/2 rows of B per k-block.
+    if (int rc = make_tmap_bf16(&ta, g.a, g.M, g.K, g.lda, 128)) return rc;
     for (int i = 0; i < 3; ++i) {
         const void *b = g.b[i < nseg ? i : 0];
-        if (int rc = make_tmap_bf16(&tb.m[i], b, g.seg_n, g.K, g.ldb, BN)) return rc;
+        if (int rc = make_tmap_bf16(&tb.m[i], b, g.seg_n, g.K, g.ldb, BN / 2)) return rc;
     }
     GemmArgs a;
     a.M = g.M;
     a.N = g.N;
     a.num_kb = (g.K + BK - 1) / BK;
     a.tiles_n = g.N / BN;
-    const int tiles_m = (g.M + BM - 1) / BM;
+    const int tiles_m = (g.M + 255) / 256;  // 256-row tiles per CTA pair
     a.num_tiles = tiles_m * a.tiles_n;
     a.seg_n = g.seg_n;
     a.bias0 = g.bias[0];
@@ -366,9 +552,19 @@ int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cud
     a.pos = g.pos;
     a.rows_per_win = g.rows_per_win;
     a.ctl = ctl;
-    const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
+    // Output tensor map for the TMA-store epilogues (32-row boxes); the conv modes write
+    // directly and get a placeholder copy of the A map.
+    CUtensorMap to = ta;
+    if (mode == GEMM_BF16 || mode == GEMM_GELU_BF16) {
+        if (int rc = make_tmap_bf16(&to, g.out, g.M, (int)g.ldo, (int)g.ldo, 32)) return rc;
+    } else if (mode == GEMM_RESID_F32) {
+        if (int rc = make_tmap_f32(&to, g.out, g.M, (int)g.ldo, (int)g.ldo, 32)) return rc;
+    }
+    const int resident = BN == 256 ? max_active_pairs<256>(num_sms) : max_active_pairs<128>(num_sms);
+    const int pairs = a.num_tiles < resident ? a.num_tiles : resident;
     count_launch();
-    return BN == 256 ? launch_mode<256>(mode, ta, tb, a, grid, s) : launch_mode<128>(mode, ta, tb, a, grid, s);
+    return BN == 256 ? launch_pair_mode<256>(mode, ta, tb, to, a, 2 * pairs, s)
+                     : launch_pair_mode<128>(mode, ta, tb, to, a, 2 * pairs, s);
 }
 
 }  // namespace wh

@@ -30,6 +30,8 @@ struct GemmDesc {
 // 2-D bf16 TMA descriptor: rows x cols (row stride ld elements), box 64 x box_rows, 128-byte
 // swizzle, zero fill outside.  Returns a WH_* code.
 int make_tmap_bf16(CUtensorMap *m, const void *ptr, long long rows, int cols, int ld, int box_rows);
+// The same for fp32 with a 32-column (128-byte) box.
+int make_tmap_f32(CUtensorMap *m, const void *ptr, long long rows, int cols, int ld, int box_rows);
 
 // Returns a WH_* code.  Encodes the tensor maps and launches the persistent tcgen05 kernel.
 int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cudaStream_t s);
