@@ -9,17 +9,18 @@
 // (128-byte swizzle).  Per key tile j and query tile t:
 //   S_t = Q_t K_j^T            tcgen05.mma M=128 N=128 K=64 into TMEM (128 fp32 columns)
 //   softmax warps (4 per tile, one query row per thread) read S_t from TMEM, keep the running
-//   row maximum m and sum l, write P = exp2((S - m) / 8 * log2 e) as bf16 into shared memory
-//   (K-major, 128-byte swizzle)
-//   O_t += P_t V_j             tcgen05.mma M=128 N=64 K=128 into TMEM (V read MN-major)
+//   row maximum m and sum l, write P = exp2((S - m) / 8 * log2 e) as bf16 pairs into TMEM
+//   O_t += P_t V_j             tcgen05.mma M=128 N=64 K=128, A = P from TMEM, V (MN-major)
+//                              from shared memory, D in TMEM
 //   O_t accumulates in TMEM across key tiles; it is rescaled (by the softmax warps) only when
 //   the running maximum grows by more than 2^8 in the exp2 domain
-// The MMA warp alternates the two query tiles so that one tile's softmax overlaps the other
+// Each query tile has its own MMA-issuing thread, so one tile's softmax overlaps the other
 // tile's MMAs.  Keys at or past n_ctx (the last tile: 1500 = 11 * 128 + 92) are masked; the
 // score matrix never leaves the SM.
 //
-// Roles: warp 0 TMA producer, warp 1 TMEM allocation + MMA issuer (warps 2-3 idle), warps
-// 4-7 softmax of tile 0, warps 8-11 softmax of tile 1 (warp w reads TMEM lanes 32 (w % 4) ..).  Every wait is bounded (DevCtl::wait_ns): on expiry
+// Roles: warp 0 TMA producer, warp 1 TMEM allocation + MMA issuer of tile 0, warp 2 MMA
+// issuer of tile 1 (warp 3 idle), warps 4-7 softmax of tile 0, warps 8-11 softmax of tile 1
+// (warp w reads TMEM lanes 32 (w % 4) .. + 31).  Every wait is bounded (DevCtl::wait_ns): on expiry
 // the block records WH_ETIMEOUT, winds down, drains its own copies and MMAs, frees TMEM.
 #include "common.cuh"
 #include "internal.h"
@@ -28,7 +29,7 @@ namespace wh {
 
 namespace {
 
-constexpr int QT = 128, KT = 128, HD = 64, NST = 3;
+constexpr int QT = 128, KT = 128, HD = 64, NST = 4;
 constexpr int THREADS = 384;
 // Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512); the producer /
 // MMA warpgroup drops to 88 and the two softmax warpgroups rise to 208:
@@ -37,13 +38,12 @@ constexpr int REG_LOW = 88, REG_HIGH = 208;
 static_assert(128 * REG_LOW + 256 * REG_HIGH <= THREADS * 168, "register split exceeds the launch total");
 constexpr int Q_BYTES = QT * HD * 2;     // 16 KB
 constexpr int KV_BYTES = KT * HD * 2;    // 16 KB
-constexpr int P_BYTES = QT * KT * 2;     // 32 KB: two K-slabs of 64 keys
 constexpr int OFF_Q = 0;
 constexpr int OFF_KV = 2 * Q_BYTES;
-constexpr int OFF_P = OFF_KV + NST * 2 * KV_BYTES;
-constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr int OFF_BAR = OFF_KV + NST * 2 * KV_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
 constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
+                                         // P0 [384,448) P1 [448,512) (bf16 pairs)
 
 struct AttnArgs {
     int n_ctx, n_head, nkv;
@@ -72,7 +72,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t *sQ = smem + OFF_Q;
     uint8_t *sKV = smem + OFF_KV;      // stage s: K at s * 32 KB, V at s * 32 KB + 16 KB
-    uint8_t *sP = smem + OFF_P;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *q_full = bars;
     uint64_t *kv_full = bars + 1;
@@ -82,7 +81,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
     uint64_t *p_full = s_free + 2;
     uint64_t *o_full = p_full + 2;
     uint64_t *drain = o_full + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -95,7 +94,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
         mbar_init(q_full, 1);
         for (int s = 0; s < NST; ++s) {
             mbar_init(kv_full + s, 1);
-            mbar_init(kv_empty + s, 1);
+            mbar_init(kv_empty + s, 2);  // one commit from each MMA issuer
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(s_full + t, 1);
@@ -104,6 +103,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
             mbar_init(o_full + t, 1);
         }
         mbar_init(drain, 1);
+        mbar_init(drain + 1, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm);
@@ -142,55 +142,51 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
         mbar_wait(q_full, 0, p.ctl);
         for (int s = 0; s < NST; ++s)
             if ((issued >> s) & 1u) mbar_wait(kv_full + s, (last_parity >> s) & 1u, p.ctl);
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer ----------------
+    } else if ((warp == 1 || warp == 2) && lane == 0) {
+        // ---------------- MMA issuers: warp 1 -> query tile 0, warp 2 -> query tile 1 ----------------
         // Per key tile j: S_t(j+1) as soon as the softmax of tile t has read S_t(j), then
-        // O_t += P_t(j) V_j once P_t(j) is in shared memory.
+        // O_t += P_t(j) V_j once P_t(j) is in TMEM.  One issuing thread per tile keeps a tile's
+        // P V from queueing behind the other tile's Q K^T.
+        const int t = warp - 1;
         constexpr uint32_t IDESC_S = idesc_bf16_f32(QT, KT);
         constexpr uint32_t IDESC_O = idesc_bf16_f32(QT, HD) | (1u << 16);  // B (V) is MN-major
-        const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV), sp = smem_u32(sP);
+        const uint32_t sq = smem_u32(sQ) + t * Q_BYTES, skv = smem_u32(sKV);
+        const uint32_t dS = tmem + 128u * t, dO = tmem + 256u + 64u * t, aP = tmem + 384u + 64u * t;
         bool ok = mbar_wait(q_full, 0, p.ctl) && mbar_wait(kv_full, 0, p.ctl);
-        auto issue_s = [&](int t, int s) {
-            const uint64_t a = sdesc_sw128(sq + t * Q_BYTES), bk = sdesc_sw128(skv + s * 2 * KV_BYTES);
+        auto issue_s = [&](int s) {
+            const uint64_t a = sdesc_sw128(sq), bk = sdesc_sw128(skv + s * 2 * KV_BYTES);
 #pragma unroll
             for (int k = 0; k < HD / 16; ++k)
-                umma_bf16(tmem + 128u * t, a + (uint64_t)(2 * k), bk + (uint64_t)(2 * k), IDESC_S, k != 0);
+                umma_bf16(dS, a + (uint64_t)(2 * k), bk + (uint64_t)(2 * k), IDESC_S, k != 0);
             umma_commit(s_full + t);
         };
         if (ok) {
             tc_fence_after();
-            issue_s(0, 0);
-            issue_s(1, 0);
+            issue_s(0);
         }
         for (int j = 0; ok && j < p.nkv; ++j) {
             const int s = j % NST;
             if (j + 1 < p.nkv) {
                 const int s1 = (j + 1) % NST;
-                ok = !*abort_flag && mbar_wait(kv_full + s1, (uint32_t)((j + 1) / NST) & 1u, p.ctl);
-                for (int t = 0; t < 2 && ok; ++t) {
-                    ok = mbar_wait(s_free + t, (uint32_t)j & 1u, p.ctl);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(t, s1);
-                }
-            }
-            for (int t = 0; t < 2 && ok; ++t) {
-                ok = !*abort_flag && mbar_wait(p_full + t, (uint32_t)j & 1u, p.ctl);
+                ok = !*abort_flag && mbar_wait(kv_full + s1, (uint32_t)((j + 1) / NST) & 1u, p.ctl) &&
+                     mbar_wait(s_free + t, (uint32_t)j & 1u, p.ctl);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t pa = sp + t * P_BYTES, vb = skv + s * 2 * KV_BYTES + KV_BYTES;
-#pragma unroll
-                for (int k = 0; k < KT / 16; ++k)
-                    umma_bf16(tmem + 256u + 64u * t, sdesc_sw128(pa + (k >> 2) * 16384) + (uint64_t)(2 * (k & 3)),
-                              sdesc_sw128_mn(vb + k * 2048), IDESC_O, (j | k) != 0);
-                umma_commit(o_full + t);
+                issue_s(s1);
             }
+            ok = !*abort_flag && mbar_wait(p_full + t, (uint32_t)j & 1u, p.ctl);
             if (!ok) break;
-            umma_commit(kv_empty + s);  // K/V stage s is free once the MMAs issued so far are done
+            tc_fence_after();
+            const uint32_t vb = skv + s * 2 * KV_BYTES + KV_BYTES;
+#pragma unroll
+            for (int k = 0; k < KT / 16; ++k)  // P (A operand) from TMEM: 16 keys = 8 columns
+                umma_bf16_tmem_a(dO, aP + 8u * k, sdesc_sw128_mn(vb + k * 2048), IDESC_O, (j | k) != 0);
+            umma_commit(o_full + t);
+            umma_commit(kv_empty + s);  // one of the two arrivals that free K/V stage s
         }
         if (!ok) *abort_flag = 1;
-        umma_commit(drain);
-        mbar_wait(drain, 0, p.ctl);
+        umma_commit(drain + t);
+        mbar_wait(drain + t, 0, p.ctl);
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_HIGH));
@@ -203,7 +199,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + 128u * t;
         const uint32_t tO = tmem + lane_off + 256u + 64u * t;
-        uint8_t *prow = sP + t * P_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+        const uint32_t tP = tmem + lane_off + 384u + 64u * t;
         const float sl2 = p.scale_log2;
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
@@ -269,27 +265,25 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
 #pragma unroll
             for (int k = 0; k < 8; ++k) ps[k] = 0.0f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int hh = 0; hh < 2; ++hh) {                   // 64 keys -> 32 packed bf16 pairs
+                uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float e = ex2(fmaf(__uint_as_float(sv[c][i]), sl2, -mc));
-                    ps[i & 7] += e;
-                    sv[c][i] = __float_as_uint(e);
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * hh + cc;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float e0 = ex2(fmaf(__uint_as_float(sv[c][i]), sl2, -mc));
+                        const float e1 = ex2(fmaf(__uint_as_float(sv[c][i + 1]), sl2, -mc));
+                        ps[i & 7] += e0;
+                        ps[(i + 1) & 7] += e1;
+                        pk[16 * cc + (i >> 1)] = pack_bf16(e0, e1);
+                    }
                 }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = c * 4 + q;               // 16-byte chunk of the 256-byte row
-                    uint8_t *dst = prow + (chunk >> 3) * 16384 + (((chunk & 7) ^ (r & 7)) << 4);
-                    uint32_t w[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        w[k] = pack_bf16(__uint_as_float(sv[c][8 * q + 2 * k]), __uint_as_float(sv[c][8 * q + 2 * k + 1]));
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
+                tmem_st32(tP + 32u * hh, pk);
             }
+            tmem_wait_st();
             l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             tc_fence_before();
-            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full + t);
         }
