@@ -53,6 +53,11 @@ struct AttnArgs {
 };
 
 __device__ __forceinline__ float ex2(float x) { return ex2_approx(x); }
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 // MN-major operand (V: rows = keys (the K dimension), 64 contiguous head dims = one 128-byte
 // swizzle atom along N): 8-row K groups 1024 bytes apart.  Only one atom along N, so the
 // leading offset is never used; it is set to the same 1024 bytes.
@@ -81,7 +86,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
     uint64_t *p_full = s_free + 2;
     uint64_t *o_full = p_full + 2;
     uint64_t *drain = o_full + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
+    uint64_t *turn = drain + 2;         // turn[t]: tile t may run its exponentials
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(turn + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -104,6 +110,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
         }
         mbar_init(drain, 1);
         mbar_init(drain + 1, 1);
+        mbar_init(turn, 4);
+        mbar_init(turn + 1, 4);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm);
@@ -203,6 +211,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
         const float sl2 = p.scale_log2;
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
+        if (t == 1 && lane == 0) mbar_arrive(turn);   // tile 0 takes the first turn
         for (int j = 0; j < p.nkv; ++j) {
             ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(s_full + t, (uint32_t)j & 1u, p.ctl));
             if (!ok) break;
@@ -229,9 +238,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(sv[c][i]));
-            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                for (int i = 0; i < 32; i += 2)
+                    pm[(i >> 1) & 7] = max3(pm[(i >> 1) & 7], __uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1]));
+            const float mx = max3(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
             const float m_new = fmaxf(m, mx);
             if (j == 0) {
                 m = m_new;
@@ -260,6 +269,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
                     tmem_wait_st();
                 }
             }
+            // Ping-pong: the two tiles take turns in the exponential section, so one tile's
+            // S load, row maximum and waits overlap the other tile's exponentials.
+            ok = __all_sync(0xffffffffu, mbar_wait(turn + t, (uint32_t)j & 1u, p.ctl));
+            if (!ok) break;
             const float mc = m * sl2;
             float ps[8];                                       // 8 independent partial sums
 #pragma unroll
@@ -281,6 +294,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
                 }
                 tmem_st32(tP + 32u * hh, pk);
             }
+            __syncwarp();
+            if (lane == 0 && (t == 0 || j + 1 < p.nkv)) mbar_arrive(turn + (1 - t));  // other tile's turn
             tmem_wait_st();
             l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             tc_fence_before();
