@@ -274,9 +274,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
             ok = __all_sync(0xffffffffu, mbar_wait(turn + t, (uint32_t)j & 1u, p.ctl));
             if (!ok) break;
             const float mc = m * sl2;
-            float ps[8];                                       // 8 independent partial sums
+            // exponentials: scale-and-subtract and the row sum two lanes at a time (packed fp32)
+            const uint64_t sl2x2 = f2_pack(sl2, sl2), nmcx2 = f2_pack(-mc, -mc);
+            uint64_t ps[4];                                    // 4 x 2 independent partial sums
 #pragma unroll
-            for (int k = 0; k < 8; ++k) ps[k] = 0.0f;
+            for (int k = 0; k < 4; ++k) ps[k] = 0ull;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {                   // 64 keys -> 32 packed bf16 pairs
                 uint32_t pk[32];
@@ -285,10 +287,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
                     const int c = 2 * hh + cc;
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        const float e0 = ex2(fmaf(__uint_as_float(sv[c][i]), sl2, -mc));
-                        const float e1 = ex2(fmaf(__uint_as_float(sv[c][i + 1]), sl2, -mc));
-                        ps[i & 7] += e0;
-                        ps[(i + 1) & 7] += e1;
+                        const uint64_t x = fma_f2(f2_pack(__uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1])),
+                                                  sl2x2, nmcx2);
+                        float x0, x1;
+                        f2_unpack(x, x0, x1);
+                        const float e0 = ex2(x0), e1 = ex2(x1);
+                        ps[(i >> 1) & 3] = add_f2(ps[(i >> 1) & 3], f2_pack(e0, e1));
                         pk[16 * cc + (i >> 1)] = pack_bf16(e0, e1);
                     }
                 }
@@ -297,7 +301,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
             __syncwarp();
             if (lane == 0 && (t == 0 || j + 1 < p.nkv)) mbar_arrive(turn + (1 - t));  // other tile's turn
             tmem_wait_st();
-            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            {
+                const uint64_t s2 = add_f2(add_f2(ps[0], ps[1]), add_f2(ps[2], ps[3]));
+                float a0, a1;
+                f2_unpack(s2, a0, a1);
+                l += a0 + a1;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full + t);

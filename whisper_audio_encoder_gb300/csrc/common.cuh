@@ -285,6 +285,26 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
+// Packed two-wide fp32 arithmetic (one instruction for two lanes of a 64-bit register pair).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // GELU(x) = x Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), the exact (erf) form.  erf is evaluated
 // with the rational approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
 // formula 7.1.26 (|error| <= 1.5e-7 for all z >= 0, odd extension for z < 0):
