@@ -322,6 +322,33 @@ __device__ __forceinline__ float gelu_erf(float x) {
     const float erf_abs = fmaf(-poly, e, 1.0f);
     return 0.5f * x * (1.0f + copysignf(erf_abs, x));
 }
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// GELU of two values at once (same formula as gelu_erf), packed fp32 where it pays.
+__device__ __forceinline__ void gelu_erf2(float &x0, float &x1) {
+    const uint64_t x = f2_pack(x0, x1);
+    const uint64_t z = f2_pack(fabsf(x0) * 0.70710678118654752f, fabsf(x1) * 0.70710678118654752f);
+    float za, zb;
+    f2_unpack(fma_f2(z, f2_pack(0.3275911f, 0.3275911f), f2_pack(1.0f, 1.0f)), za, zb);
+    const uint64_t t = f2_pack(rcp_approx(za), rcp_approx(zb));
+    uint64_t poly = fma_f2(t, f2_pack(1.061405429f, 1.061405429f), f2_pack(-1.453152027f, -1.453152027f));
+    poly = fma_f2(t, poly, f2_pack(1.421413741f, 1.421413741f));
+    poly = fma_f2(t, poly, f2_pack(-0.284496736f, -0.284496736f));
+    poly = fma_f2(t, poly, f2_pack(0.254829592f, 0.254829592f));
+    poly = mul_f2(poly, t);
+    float ea, eb;
+    f2_unpack(mul_f2(mul_f2(z, z), f2_pack(-1.4426950408889634f, -1.4426950408889634f)), ea, eb);
+    const uint64_t e = f2_pack(ex2_approx(ea), ex2_approx(eb));
+    float ra, rb;  // |erf|
+    f2_unpack(fma_f2(poly, f2_pack(-1.0f, -1.0f) /* -poly */, f2_pack(0.0f, 0.0f)), ra, rb);
+    f2_unpack(fma_f2(f2_pack(ra, rb), e, f2_pack(1.0f, 1.0f)), ra, rb);
+    const uint64_t one_plus = f2_pack(1.0f + copysignf(ra, x0), 1.0f + copysignf(rb, x1));
+    f2_unpack(mul_f2(mul_f2(x, f2_pack(0.5f, 0.5f)), one_plus), x0, x1);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);

@@ -168,7 +168,7 @@ __device__ __forceinline__ void bias_act(const GemmArgs &p, int col, const uint3
     }
     if constexpr (MODE == GEMM_GELU_BF16) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+        for (int j = 0; j < 32; j += 2) gelu_erf2(v[j], v[j + 1]);
     }
 }
 

@@ -1,6 +1,6 @@
 // LayerNorm ("whisper 0.9.0 API", kernels.nu: LayerNorm, not RMSNorm -- it subtracts the
 // mean and it has a bias): y = (x - mean) / sqrt(var + 1e-5) * g + b, biased variance.
-// One warp per row, the row held in registers (d <= 2048: <= 32 float2 per lane), two
+// One warp per row, the row held in registers (d <= 2048: <= 16 float4 per lane), two
 // passes over the registers (mean, then centred variance), warp-shuffle reductions.
 // HBM-bound: reads 4 d bytes and writes 2 d (bf16) or 4 d (fp32) bytes per row.
 #include "common.cuh"
@@ -11,8 +11,9 @@ namespace wh {
 namespace {
 
 constexpr int LN_THREADS = 256;
-constexpr int MAXV = 32;  // float2 per lane
+constexpr int MAXV = 16;  // float4 per lane: d <= 2048
 
+// d a multiple of 128: each lane holds d / 128 float4 (16-byte loads and stores).
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restrict__ x, int rows, int d,
                                                           const float *__restrict__ g,
@@ -20,12 +21,62 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restric
     const int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const int nv = d >> 6;
-    const float2 *xr = reinterpret_cast<const float2 *>(x + (long long)row * d);
-    float2 v[MAXV];
-    float s = 0.0f;
+    const int nv = d >> 7;
+    const float4 *xr = reinterpret_cast<const float4 *>(x + (long long)row * d);
+    float4 v[MAXV];
+    float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < MAXV; ++i)
+        if (i < nv) v[i] = __ldg(xr + i * 32 + lane);
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i)
+        if (i < nv) {
+            s0 += v[i].x + v[i].y;
+            s1 += v[i].z + v[i].w;
+        }
+    const float mean = warp_sum(s0 + s1) / (float)d;
+    float q0 = 0.0f, q1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i)
+        if (i < nv) {
+            const float a = v[i].x - mean, bb = v[i].y - mean, c = v[i].z - mean, e = v[i].w - mean;
+            q0 = fmaf(a, a, fmaf(bb, bb, q0));
+            q1 = fmaf(c, c, fmaf(e, e, q1));
+        }
+    const float rstd = 1.0f / sqrtf(warp_sum(q0 + q1) / (float)d + 1e-5f);
+    const float4 *g4 = reinterpret_cast<const float4 *>(g);
+    const float4 *b4 = reinterpret_cast<const float4 *>(b);
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i)
+        if (i < nv) {
+            const int c = i * 32 + lane;
+            const float4 gg = __ldg(g4 + c), bb = __ldg(b4 + c);
+            const float o0 = (v[i].x - mean) * rstd * gg.x + bb.x;
+            const float o1 = (v[i].y - mean) * rstd * gg.y + bb.y;
+            const float o2 = (v[i].z - mean) * rstd * gg.z + bb.z;
+            const float o3 = (v[i].w - mean) * rstd * gg.w + bb.w;
+            if constexpr (OUT_BF16) {
+                reinterpret_cast<uint2 *>(y)[(long long)row * (d >> 2) + c] = make_uint2(pack_bf16(o0, o1), pack_bf16(o2, o3));
+            } else {
+                reinterpret_cast<float4 *>(y)[(long long)row * (d >> 2) + c] = make_float4(o0, o1, o2, o3);
+            }
+        }
+}
+
+// d a multiple of 64 but not of 128: float2 per lane.
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(LN_THREADS) k_layernorm64(const float *__restrict__ x, int rows, int d,
+                                                            const float *__restrict__ g,
+                                                            const float *__restrict__ b, void *__restrict__ y) {
+    const int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int nv = d >> 6;
+    const float2 *xr = reinterpret_cast<const float2 *>(x + (long long)row * d);
+    float2 v[2 * MAXV];
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 2 * MAXV; ++i)
         if (i < nv) {
             v[i] = __ldg(xr + i * 32 + lane);
             s += v[i].x + v[i].y;
@@ -33,7 +84,7 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restric
     const float mean = warp_sum(s) / (float)d;
     float q = 0.0f;
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i)
+    for (int i = 0; i < 2 * MAXV; ++i)
         if (i < nv) {
             const float dx = v[i].x - mean, dy = v[i].y - mean;
             q = fmaf(dx, dx, fmaf(dy, dy, q));
@@ -42,7 +93,7 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restric
     const float2 *g2 = reinterpret_cast<const float2 *>(g);
     const float2 *b2 = reinterpret_cast<const float2 *>(b);
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i)
+    for (int i = 0; i < 2 * MAXV; ++i)
         if (i < nv) {
             const int c = i * 32 + lane;
             const float2 gg = __ldg(g2 + c), bb = __ldg(b2 + c);
@@ -61,12 +112,19 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restric
 int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,
                      cudaStream_t s) {
     if (rows <= 0) return WH_OK;
-    if (d % 64 != 0 || d < 64 || d > 64 * MAXV) return WH_EINVAL;
+    if (d % 64 != 0 || d < 64 || d > 128 * MAXV) return WH_EINVAL;
     const int grid = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
-    if (y_bf16)
-        k_layernorm<true><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
-    else
-        k_layernorm<false><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+    if (d % 128 == 0) {
+        if (y_bf16)
+            k_layernorm<true><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+        else
+            k_layernorm<false><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+    } else {
+        if (y_bf16)
+            k_layernorm64<true><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+        else
+            k_layernorm64<false><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+    }
     count_launch();
     return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
 }
