@@ -86,8 +86,8 @@ typedef struct {
  *         wh_encode: "mel is 3000 x n_mels, row-major (a frame is contiguous)").
  *   workspace  device scratch of at least wh_frontend_workspace(batch) bytes, 16-byte aligned
  *         (the per-window maxima); contents need not be initialised.
- * Errors: WH_EINVAL (null pointer with batch > 0, n < 0, batch < 0, n_mels not 80/128),
- *         WH_ENOSPC (workspace too small), WH_ECUDA.  batch == 0 is a no-op.
+ * Errors: WH_EINVAL (null pointer with batch > 0, n < 0, batch < 0 or > 65535, n_mels not
+ *         80/128), WH_ENOSPC (workspace too small), WH_ECUDA.  batch == 0 is a no-op.
  * ------------------------------------------------------------------------------------ */
 size_t wh_frontend_workspace(int batch);
 int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel,

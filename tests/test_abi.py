@@ -88,6 +88,7 @@ def test_frontend_rejects_bad_arguments(L):
     assert L.wh_frontend(FAKE, 480000, 1, 81, FAKE, FAKE, 256, None) == wh.WH_EINVAL
     assert L.wh_frontend(FAKE, -1, 1, 80, FAKE, FAKE, 256, None) == wh.WH_EINVAL
     assert L.wh_frontend(FAKE, 480000, -1, 80, FAKE, FAKE, 256, None) == wh.WH_EINVAL
+    assert L.wh_frontend(FAKE, 480000, 65536, 80, FAKE, FAKE, 1 << 30, None) == wh.WH_EINVAL
     assert L.wh_frontend(None, 480000, 1, 80, FAKE, FAKE, 256, None) == wh.WH_EINVAL
     assert L.wh_frontend(FAKE, 480000, 1, 80, None, FAKE, 256, None) == wh.WH_EINVAL
     assert L.wh_frontend(FAKE, 480000, 1, 80, FAKE, None, 256, None) == wh.WH_EINVAL

@@ -4,7 +4,7 @@
 // power re^2 + im^2 on the 201 x 3000 grid, Slaney area-normalised mel filters, log10,
 // clamp at (window maximum - 8) and (x + 4) / 4.
 //
-// Kernel 1 (k_logmel): one block = 32 consecutive frames of one window.  The 5360 samples
+// Kernel 1 (k_logmel): one block = 30 consecutive frames of one window.  The 5040 samples
 // the frames touch are staged once in shared memory (coalesced; reflect and zero-extension
 // applied while loading).  Each real 400-point frame x is transformed as one complex
 // 200-point FFT of z[m] = x[2m] + i x[2m+1] (decomposed 200 = 8 x 25, the 25-point part as
@@ -25,12 +25,14 @@ namespace wh {
 namespace {
 
 constexpr int N_FFT = 400, HOP = 160, N_FRAMES = 3000, N_SAMPLES = 480000, N_BINS = 201;
-constexpr int FB = 32;                          // frames per block
+constexpr int FB = 30;                          // frames per block: 3000 = 100 x 30
 constexpr int THREADS = 256;
-constexpr int SEG = FB * HOP + (N_FFT - HOP);   // 5360 staged samples
-constexpr int ZSTRIDE = 201;                    // complex slots per frame (200 used, padded)
+constexpr int SEG = FB * HOP + (N_FFT - HOP);   // 5040 staged samples
+constexpr int ZSTRIDE = 200;                    // complex slots per frame
 constexpr int MAXW = 512;                       // mel filter nonzeros (<= 2 per bin)
-constexpr size_t SMEM = (size_t)SEG * 4 + (size_t)FB * ZSTRIDE * 8 + (size_t)FB * N_BINS * 4;
+// The staged samples are dead after stage A, so the power spectrum reuses their space.
+constexpr int SEGP = SEG > FB * N_BINS ? SEG : FB * N_BINS;
+constexpr size_t SMEM = (size_t)SEGP * 4 + (size_t)FB * ZSTRIDE * 8;
 
 __device__ float g_hann[N_FFT];
 __device__ float2 g_tw[N_FFT];          // W400^j = (cos, -sin)(2 pi j / 400)
@@ -102,9 +104,9 @@ __global__ void __launch_bounds__(THREADS) k_logmel(const float *__restrict__ pc
                                                     int table, float *__restrict__ mel,
                                                     uint32_t *__restrict__ wmax) {
     extern __shared__ float4 smem4[];
-    float *seg = reinterpret_cast<float *>(smem4);
-    float2 *Z = reinterpret_cast<float2 *>(seg + SEG);   // [FB][ZSTRIDE]
-    float *P = reinterpret_cast<float *>(Z + FB * ZSTRIDE);  // [FB][201]
+    float *seg = reinterpret_cast<float *>(smem4);       // staged samples, then the power [FB][201]
+    float2 *Z = reinterpret_cast<float2 *>(seg + SEGP);  // [FB][ZSTRIDE]
+    float *P = seg;
     __shared__ float red[THREADS / 32];
 
     const int tid = threadIdx.x;
@@ -113,12 +115,21 @@ __global__ void __launch_bounds__(THREADS) k_logmel(const float *__restrict__ pc
     const int nf = min(FB, N_FRAMES - t0);
     const float *x = pcm + (long long)b * n;
 
-    // Stage samples 160 t0 - 200 ... (pad/truncate to 480000, then reflect by 200).
-    for (int j = tid; j < SEG; j += THREADS) {
-        int s = HOP * t0 - N_FFT / 2 + j;
-        s = s < 0 ? -s : s;
-        s = s > N_SAMPLES - 1 ? 2 * (N_SAMPLES - 1) - s : s;
-        seg[j] = (s < n) ? __ldg(x + s) : 0.0f;
+    // Stage samples 160 t0 - 200 ... (pad/truncate to 480000, then reflect by 200).  Blocks
+    // whose span lies inside the clip and is 16-byte aligned copy with float4 loads.
+    const long long s0 = (long long)HOP * t0 - N_FFT / 2;
+    const long long lim = n < N_SAMPLES ? n : N_SAMPLES;
+    if (s0 >= 0 && s0 + SEG <= lim && ((reinterpret_cast<uintptr_t>(x + s0) & 15) == 0)) {
+        const float4 *src = reinterpret_cast<const float4 *>(x + s0);
+        float4 *dst = reinterpret_cast<float4 *>(seg);
+        for (int j = tid; j < SEG / 4; j += THREADS) dst[j] = __ldg(src + j);
+    } else {
+        for (int j = tid; j < SEG; j += THREADS) {
+            int si = (int)s0 + j;
+            si = si < 0 ? -si : si;
+            si = si > N_SAMPLES - 1 ? 2 * (N_SAMPLES - 1) - si : si;
+            seg[j] = (si < n) ? __ldg(x + si) : 0.0f;
+        }
     }
     __syncthreads();
 
@@ -176,36 +187,46 @@ __global__ void __launch_bounds__(THREADS) k_logmel(const float *__restrict__ pc
     }
     __syncthreads();
 
-    // Stage C: real spectrum and power.  E = (Z[k] + conj Z[-k]) / 2, O = -i (Z[k] - conj Z[-k]) / 2,
-    // X[k] = E + W400^k O, P = |X|^2, k = 0..200.
-    for (int it = tid; it < nf * N_BINS; it += THREADS) {
-        const int f = it / N_BINS, k = it - f * N_BINS;
+    // Stage C: real spectrum and power, one warp per frame, lanes over bins.
+    // E = (Z[k] + conj Z[-k]) / 2, O = -i (Z[k] - conj Z[-k]) / 2, X[k] = E + W400^k O, P = |X|^2.
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int f = warp; f < nf; f += THREADS / 32) {
         const float2 *zf = Z + f * ZSTRIDE;
-        const float2 zk = zf[k == 200 ? 0 : k];
-        const float2 zm = zf[k == 0 ? 0 : 200 - k];
-        const float2 e = make_float2(0.5f * (zk.x + zm.x), 0.5f * (zk.y - zm.y));
-        const float2 o = make_float2(0.5f * (zk.y + zm.y), -0.5f * (zk.x - zm.x));
-        const float2 X = cadd(e, cmul(g_tw[k], o));
-        P[f * N_BINS + k] = X.x * X.x + X.y * X.y;
+        float *pf = P + f * N_BINS;
+        for (int k = lane; k < N_BINS; k += 32) {
+            const float2 zk = zf[k == 200 ? 0 : k];
+            const float2 zm = zf[k == 0 ? 0 : 200 - k];
+            const float2 e = make_float2(0.5f * (zk.x + zm.x), 0.5f * (zk.y - zm.y));
+            const float2 o = make_float2(0.5f * (zk.y + zm.y), -0.5f * (zk.x - zm.x));
+            const float2 X = cadd(e, cmul(g_tw[k], o));
+            pf[k] = X.x * X.x + X.y * X.y;
+        }
     }
     __syncthreads();
 
     // Stage D: mel projection, log10 with floor 1e-10, frame-major store, block maximum.
+    // One warp per frame, lanes over mel bins (coalesced stores).
     float lmax = -INFINITY;
-    float *out = mel + ((long long)b * N_FRAMES + t0) * n_mels;
-    for (int it = tid; it < nf * n_mels; it += THREADS) {
-        const int f = it / n_mels, m = it - f * n_mels;
-        const int k0 = g_mel_start[table][m], len = g_mel_len[table][m];
-        const float *wm = g_mel_w[table] + g_mel_off[table][m];
-        const float *pf = P + f * N_BINS + k0;
-        float s = 0.0f;
-        for (int i = 0; i < len; ++i) s = fmaf(wm[i], pf[i], s);
-        const float lg = log10f(fmaxf(s, 1e-10f));
-        out[it] = lg;
-        lmax = fmaxf(lmax, lg);
+    const int *mstart = g_mel_start[table], *mlen = g_mel_len[table], *moff = g_mel_off[table];
+    const float *mw = g_mel_w[table];
+    for (int f = warp; f < nf; f += THREADS / 32) {
+        const float *pf = P + f * N_BINS;
+        float *out = mel + ((long long)b * N_FRAMES + t0 + f) * n_mels;
+        for (int m = lane; m < n_mels; m += 32) {
+            const int k0 = mstart[m], len = mlen[m];
+            const float *wm = mw + moff[m];
+            float acc = 0.0f;
+            for (int i = 0; i < len; ++i) acc = fmaf(wm[i], pf[k0 + i], acc);
+            // log10 via the hardware log2 (log10 x = log2 x * log10 2); at the floor exactly -10.
+            float lg2;
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg2) : "f"(acc));
+            const float lg = acc > 1e-10f ? lg2 * 0.30102999566398120f : -10.0f;
+            out[m] = lg;
+            lmax = fmaxf(lmax, lg);
+        }
     }
     lmax = warp_max(lmax);
-    if ((tid & 31) == 0) red[tid >> 5] = lmax;
+    if (lane == 0) red[warp] = lmax;
     __syncthreads();
     if (tid < 32) {
         float v = tid < THREADS / 32 ? red[tid] : -INFINITY;
@@ -214,17 +235,19 @@ __global__ void __launch_bounds__(THREADS) k_logmel(const float *__restrict__ pc
     }
 }
 
-__global__ void __launch_bounds__(256) k_clamp(float4 *__restrict__ mel, long long per_window4, long long total4,
+// grid.y = window: mel[b] = (max(mel[b], g_b - 8) + 4) / 4, float4 at a time.
+__global__ void __launch_bounds__(256) k_clamp(float4 *__restrict__ mel, int per_window4,
                                                const uint32_t *__restrict__ wmax) {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total4;
-         i += (long long)gridDim.x * blockDim.x) {
-        const float floor = key2f(wmax[i / per_window4]) - 8.0f;
-        float4 v = mel[i];
+    const int b = blockIdx.y;
+    const float floor = key2f(wmax[b]) - 8.0f;
+    float4 *w = mel + (long long)b * per_window4;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < per_window4; i += gridDim.x * blockDim.x) {
+        float4 v = w[i];
         v.x = (fmaxf(v.x, floor) + 4.0f) * 0.25f;
         v.y = (fmaxf(v.y, floor) + 4.0f) * 0.25f;
         v.z = (fmaxf(v.z, floor) + 4.0f) * 0.25f;
         v.w = (fmaxf(v.w, floor) + 4.0f) * 0.25f;
-        mel[i] = v;
+        w[i] = v;
     }
 }
 
@@ -319,10 +342,9 @@ int frontend_launch(const float *pcm, int64_t n, int batch, int n_mels, float *m
     if (cudaMemsetAsync(wmax, 0, sizeof(uint32_t) * (size_t)batch, s) != cudaSuccess) return WH_ECUDA;
     dim3 grid((N_FRAMES + FB - 1) / FB, batch);
     k_logmel<<<grid, THREADS, SMEM, s>>>(pcm, (long long)n, n_mels, n_mels == 128 ? 1 : 0, mel, wmax);
-    const long long per4 = (long long)N_FRAMES * n_mels / 4, total4 = per4 * batch;
-    long long blocks = (total4 + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    k_clamp<<<(int)blocks, 256, 0, s>>>(reinterpret_cast<float4 *>(mel), per4, total4, wmax);
+    const int per4 = N_FRAMES * n_mels / 4;
+    dim3 cgrid((per4 + 255) / 256, batch);
+    k_clamp<<<cgrid, 256, 0, s>>>(reinterpret_cast<float4 *>(mel), per4, wmax);
     count_launch(2);
     return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
 }

@@ -227,7 +227,7 @@ size_t wh_frontend_workspace(int batch) { return batch <= 0 ? 0 : up256(sizeof(u
 
 int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel, void *workspace, size_t ws_bytes,
                 void *stream) {
-    if (batch < 0 || n < 0 || (n_mels != 80 && n_mels != 128)) return WH_EINVAL;
+    if (batch < 0 || batch > 65535 || n < 0 || (n_mels != 80 && n_mels != 128)) return WH_EINVAL;
     if (batch == 0) return WH_OK;
     if (!mel || !workspace || (n > 0 && !pcm)) return WH_EINVAL;
     if (!aligned(mel, 16) || !aligned(workspace, 16)) return WH_EINVAL;
