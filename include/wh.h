@@ -131,6 +131,24 @@ int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weight
               float *out, void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Recorded passes ("whisper 0.9.0 API" README, implementation notes: the encoder is
+ * "recorded once when the model opens and replayed").  wh_graph_capture records one
+ * wh_frontend + wh_encode pass on `stream` into a CUDA graph (arguments exactly as for those
+ * two calls; mel is the log-mel buffer between them).  wh_graph_launch replays it on any
+ * stream: the same buffers are read and written, so refresh pcm in place and replay.  The
+ * graph keeps the pointers it was recorded with; buffers must stay alive until
+ * wh_graph_destroy.  `stream` must not be the legacy default stream (NULL).
+ * Errors: as wh_frontend / wh_encode; WH_EINVAL for a NULL stream or graph; WH_ECUDA if the
+ * capture or instantiation fails.
+ * ------------------------------------------------------------------------------------ */
+typedef struct wh_graph wh_graph;
+int wh_graph_capture(const float *pcm, int64_t n, int batch, const wh_config *cfg, const wh_weights *w,
+                     float *mel, float *out, void *fe_ws, size_t fe_ws_bytes, void *enc_ws, size_t enc_ws_bytes,
+                     void *stream, wh_graph **graph);
+int wh_graph_launch(wh_graph *graph, void *stream);
+int wh_graph_destroy(wh_graph *graph);
+
+/* ---------------------------------------------------------------------------------------
  * Single steps of the encoder, exposed for testing and for callers that compose their own
  * pipeline.  Same conventions as above.
  * ------------------------------------------------------------------------------------ */

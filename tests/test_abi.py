@@ -108,6 +108,18 @@ def test_single_step_entry_points_reject_bad_shapes(L):
     assert L.wh_selftest_timeout(2_000_000_000, None) == wh.WH_EINVAL
 
 
+def test_graph_entry_points_reject_bad_arguments(L):
+    c = wh.wh_config(80, 384, 6, 0, 1536)
+    w = wh.wh_weights()
+    h = ctypes.c_void_p()
+    assert L.wh_graph_capture(FAKE, 480000, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, FAKE, 256, FAKE,
+                              1 << 30, None, ctypes.byref(h)) == wh.WH_EINVAL          # default stream
+    assert L.wh_graph_capture(FAKE, 480000, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, FAKE, 256, FAKE,
+                              1 << 30, FAKE, None) == wh.WH_EINVAL                     # no graph slot
+    assert L.wh_graph_launch(None, None) == wh.WH_EINVAL
+    assert L.wh_graph_destroy(None) == wh.WH_EINVAL
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_no_device_is_reported(L):
     assert L.wh_frontend(FAKE, 480000, 1, 80, FAKE, FAKE, 256, None) == wh.WH_ENODEV

@@ -1,0 +1,43 @@
+"""Recorded passes (wh_graph_capture / wh_graph_launch): a replay gives exactly the memory of
+a direct wh_frontend + wh_encode call on the same buffers, also after the PCM is refreshed in
+place between replays."""
+import numpy as np
+import pytest
+import torch
+
+from whisper_audio_encoder_gb300 import build, configs, synth, wh
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    build.build()
+    wh.lib()
+
+
+def test_graph_replay_equals_direct_calls():
+    cfg = configs.CONFIGS[1]
+    enc = wh.Encoder(cfg, synth.weights(cfg))
+    first = torch.from_numpy(synth.waveforms(cfg)).cuda()
+    second = torch.from_numpy(synth.waveforms(cfg, windows=range(8, 16))).cuda()
+    B = cfg.batch
+    pcm = first.clone()
+    mel = torch.empty(B, 3000, cfg.n_mels, device="cuda")
+    out = torch.empty(B, 1500, cfg.d_model, device="cuda")
+    stream = torch.cuda.Stream()
+    graph = enc.capture(pcm, mel, out, stream)
+    refs = []
+    for src in (first, second):
+        refs.append(enc.forward(src.clone()).cpu().numpy())
+    torch.cuda.synchronize()
+    for src, ref in zip((first, second), refs):
+        with torch.cuda.stream(stream):
+            pcm.copy_(src)
+            graph.launch(stream)
+        stream.synchronize()
+        assert np.array_equal(out.cpu().numpy(), ref)
+    assert wh.wh_status() == wh.WH_OK
+    graph.destroy()

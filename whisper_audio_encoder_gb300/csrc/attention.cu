@@ -349,6 +349,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
 
 }  // namespace
 
+int attention_prepare() {
+    return cudaFuncSetAttribute(k_attention_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess
+               ? WH_OK
+               : WH_ECUDA;
+}
+
 int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
                      cudaStream_t s) {
     if (batch <= 0) return WH_OK;
@@ -362,8 +368,6 @@ int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *ou
     a.out = reinterpret_cast<__nv_bfloat16 *>(out);
     a.scale_log2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
     a.ctl = ctl;
-    if (cudaFuncSetAttribute(k_attention_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
-        return WH_ECUDA;
     dim3 grid((n_ctx + 2 * QT - 1) / (2 * QT), n_head, batch);
     k_attention_tc<<<grid, THREADS, SMEM_BYTES, s>>>(tm, a);
     count_launch();

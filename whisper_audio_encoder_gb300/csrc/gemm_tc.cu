@@ -416,10 +416,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 template <int BN, int MODE>
 int launch_pair_t(const CUtensorMap &ta, const TmapB &tb, const CUtensorMap &to, const GemmArgs &a, int grid,
                   cudaStream_t s) {
-    auto kern = k_gemm2<BN, MODE>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<BN>::SMEM_BYTES) !=
-        cudaSuccess)
-        return WH_ECUDA;
+    auto kern = k_gemm2<BN, MODE>;  // shared-memory attribute set once per device (gemm_prepare)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
@@ -465,6 +462,14 @@ int max_active_pairs(int num_sms) {
     }
     cached[dev] = n;
     return n;
+}
+
+template <int BN, int MODE>
+int set_attr() {
+    return cudaFuncSetAttribute(k_gemm2<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg2<BN>::SMEM_BYTES) == cudaSuccess
+               ? WH_OK
+               : WH_ECUDA;
 }
 
 template <int BN>
@@ -520,6 +525,18 @@ int make_tmap_bf16(CUtensorMap *m, const void *ptr, long long rows, int cols, in
 }
 int make_tmap_f32(CUtensorMap *m, const void *ptr, long long rows, int cols, int ld, int box_rows) {
     return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, rows, cols, ld, 32, box_rows);
+}
+
+int gemm_prepare(int num_sms) {
+    int rc = 0;
+    rc |= set_attr<256, GEMM_BF16>() | set_attr<256, GEMM_GELU_BF16>() | set_attr<256, GEMM_RESID_F32>();
+    rc |= set_attr<256, GEMM_CONV1>() | set_attr<256, GEMM_CONV2>();
+    rc |= set_attr<128, GEMM_BF16>() | set_attr<128, GEMM_GELU_BF16>() | set_attr<128, GEMM_RESID_F32>();
+    rc |= set_attr<128, GEMM_CONV1>() | set_attr<128, GEMM_CONV2>();
+    if (rc) return WH_ECUDA;
+    max_active_pairs<256>(num_sms);
+    max_active_pairs<128>(num_sms);
+    return tmap_encoder_ready();
 }
 
 int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cudaStream_t s) {

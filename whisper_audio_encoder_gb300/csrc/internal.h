@@ -35,6 +35,9 @@ int make_tmap_f32(CUtensorMap *m, const void *ptr, long long rows, int cols, int
 
 // Returns a WH_* code.  Encodes the tensor maps and launches the persistent tcgen05 kernel.
 int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cudaStream_t s);
+// Host-side set-up of every GEMM variant (function attributes, resident-pair counts) on the
+// current device, so that later launches do no set-up work (e.g. inside a stream capture).
+int gemm_prepare(int num_sms);
 
 // ---- front end (frontend.cu) -------------------------------------------------------------
 int frontend_init_tables();   // once per device (current device)
@@ -46,6 +49,7 @@ int layernorm_launch(const float *x, int rows, int d, const float *g, const floa
                      cudaStream_t s);
 int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
                      cudaStream_t s);
+int attention_prepare();
 int stem_im2col_launch(const float *mel, int batch, int n_mels, void *a1, cudaStream_t s);
 int pack_conv_weight_launch(const void *w, int c_out, int c_in, void *wp, cudaStream_t s);
 int selftest_timeout_launch(const DevCtl &ctl, cudaStream_t s);

@@ -56,6 +56,8 @@ int ensure_device(DevState **out) {
         if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return WH_ECUDA;
         if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return WH_ECUDA;
         if (int rc = frontend_init_tables()) return rc;
+        if (int rc = gemm_prepare(st.num_sms)) return rc;
+        if (int rc = attention_prepare()) return rc;
         st.status = static_cast<int *>(p);
         st.ready = true;
     }
@@ -377,6 +379,71 @@ int wh_selftest_timeout(uint64_t limit_ns, void *stream) {
     DevState *st;
     if (int rc = ensure_device(&st)) return rc;
     return selftest_timeout_launch(ctl_of(st, limit_ns), static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+struct wh_graph {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+extern "C" {
+
+int wh_graph_capture(const float *pcm, int64_t n, int batch, const wh_config *cfg, const wh_weights *w, float *mel,
+                     float *out, void *fe_ws, size_t fe_ws_bytes, void *enc_ws, size_t enc_ws_bytes, void *stream,
+                     wh_graph **graph) {
+    if (!graph || !stream || batch <= 0) return WH_EINVAL;
+    *graph = nullptr;
+    DevState *st;
+    if (int rc = ensure_device(&st)) return rc;  // constant tables and kernel set-up, outside the capture
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool tracing;
+    {
+        std::lock_guard<std::mutex> lk(g_tr_mu);
+        tracing = g_tr_on;
+        g_tr_on = false;  // no event records inside the recorded pass
+    }
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGetLastError();
+        g_tr_on = tracing;
+        return WH_ECUDA;
+    }
+    int rc = wh_frontend(pcm, n, batch, cfg ? cfg->n_mels : 0, mel, fe_ws, fe_ws_bytes, stream);
+    if (rc == WH_OK) rc = wh_encode(mel, batch, cfg, w, out, enc_ws, enc_ws_bytes, stream);
+    cudaGraph_t g = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(s, &g);
+    {
+        std::lock_guard<std::mutex> lk(g_tr_mu);
+        g_tr_on = tracing;
+    }
+    if (rc != WH_OK || ec != cudaSuccess || g == nullptr) {
+        if (g) cudaGraphDestroy(g);
+        cudaGetLastError();
+        return rc != WH_OK ? rc : WH_ECUDA;
+    }
+    cudaGraphExec_t e = nullptr;
+    if (cudaGraphInstantiate(&e, g, 0) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        cudaGetLastError();
+        return WH_ECUDA;
+    }
+    *graph = new wh_graph{g, e};
+    return WH_OK;
+}
+
+int wh_graph_launch(wh_graph *graph, void *stream) {
+    if (!graph) return WH_EINVAL;
+    count_launch();
+    return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? WH_OK : WH_ECUDA;
+}
+
+int wh_graph_destroy(wh_graph *graph) {
+    if (!graph) return WH_EINVAL;
+    cudaGraphExecDestroy(graph->exec);
+    cudaGraphDestroy(graph->graph);
+    delete graph;
+    return WH_OK;
 }
 
 int wh_trace_enable(int on) {

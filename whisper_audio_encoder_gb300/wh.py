@@ -74,6 +74,11 @@ def lib():
         "wh_trace_enable": (ctypes.c_int, [ctypes.c_int]),
         "wh_trace_read": (ctypes.c_int, [ctypes.POINTER(wh_trace_stat), ctypes.c_int]),
         "wh_launch_count": (ctypes.c_int64, []),
+        "wh_graph_capture": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int, ctypes.POINTER(wh_config),
+                                            ctypes.POINTER(wh_weights), _p, _p, _p, ctypes.c_size_t, _p,
+                                            ctypes.c_size_t, _p, ctypes.POINTER(ctypes.c_void_p)]),
+        "wh_graph_launch": (ctypes.c_int, [_p, _p]),
+        "wh_graph_destroy": (ctypes.c_int, [_p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -259,6 +264,20 @@ class Encoder:
                           stream=stream)
         return self.wh_encode(mel, out=out, stream=stream)
 
+    def capture(self, pcm, mel, out, stream):
+        """Records one front end + encoder pass over these device buffers (wh_graph_capture).
+        `stream` is a torch.cuda.Stream other than the default stream; replay with
+        Graph.launch(); refresh `pcm` in place between replays."""
+        batch, n = pcm.shape
+        ws = self.workspace(batch)
+        fe = self.frontend_workspace(batch)
+        h = ctypes.c_void_p()
+        rc = lib().wh_graph_capture(_ptr(pcm), n, batch, ctypes.byref(self.c_cfg), ctypes.byref(self.c_w), _ptr(mel),
+                                    _ptr(out), _ptr(fe), fe.numel(), _ptr(ws), ws.numel(), _stream(stream),
+                                    ctypes.byref(h))
+        _check(rc, "wh_graph_capture")
+        return Graph(h, (pcm, mel, out, ws, fe))
+
     def encode_from_host(self, pcm_host, out_host, pcm_dev, mel, out_dev, stream=None):
         """End to end from pinned host memory: copy PCM in, front end + encoder, copy the
         memory out (all on one stream)."""
@@ -266,3 +285,25 @@ class Encoder:
         self.forward(pcm_dev, mel=mel, out=out_dev, stream=stream)
         out_host.copy_(out_dev, non_blocking=True)
         return out_host
+
+
+class Graph:
+    """A recorded front end + encoder pass (wh_graph_*); keeps its buffers alive."""
+
+    def __init__(self, handle, keep):
+        self._h = handle
+        self._keep = keep
+
+    def launch(self, stream=None):
+        _check(lib().wh_graph_launch(self._h, _stream(stream)), "wh_graph_launch")
+
+    def destroy(self):
+        if self._h:
+            lib().wh_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
