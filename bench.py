@@ -199,11 +199,17 @@ KERNEL_SOURCES = {"gemm_fc1": ["gemm_tc.cu", "common.cuh"], "attention": ["atten
 
 
 def _sources_hash(files):
+    """sha256 of the kernel's sources with comments and blank space removed, so that an edit
+    of a comment keeps the record and any change of code drops it."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "whisper_audio_encoder_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "whisper_audio_encoder_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

@@ -4,8 +4,10 @@
 // "How Audio Becomes Words", section "The Encoder: Understand Once": the full 1500 x 1500
 // square, no mask, no RoPE).
 //
-// One CTA = two 128-query tiles (t = 0, 1) of one (window, head); keys stream through in
-// tiles of 128.  q/k/v are read straight from the QKV projection's output [rows][3 D] by TMA
+// Work item = two 128-query tiles (t = 0, 1) of one (window, head); keys stream through in
+// tiles of 128.  One persistent CTA per SM walks the items (window-major, so CTAs running at
+// the same time share K/V in L2); the next item's loads and first Q K^T overlap the current
+// item's last steps.  q/k/v are read straight from the QKV projection's output [rows][3 D] by TMA
 // (128-byte swizzle).  Per key tile j and query tile t:
 //   S_t = Q_t K_j^T            tcgen05.mma M=128 N=128 K=64 into TMEM (128 fp32 columns)
 //   softmax warps (4 per tile, one query row per thread) read S_t from TMEM, keep the running
@@ -47,6 +49,7 @@ constexpr uint32_t TMEM_COLS = 512;      // S0 [0,128) S1 [128,256) O0 [256,320)
 
 struct AttnArgs {
     int n_ctx, n_head, nkv;
+    int n_qblk, n_items;  // work items: (window, head, block of 2 query tiles), window-major
     __nv_bfloat16 *out;
     float scale_log2;
     DevCtl ctl;
@@ -79,7 +82,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
     uint8_t *sKV = smem + OFF_KV;      // stage s: K at s * 32 KB, V at s * 32 KB + 16 KB
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *q_full = bars;
-    uint64_t *kv_full = bars + 1;
+    uint64_t *q_empty = q_full + 1;     // both issuers' last Q K^T of an item has completed
+    uint64_t *kv_full = q_empty + 1;
     uint64_t *kv_empty = kv_full + NST;
     uint64_t *s_full = kv_empty + NST;
     uint64_t *s_free = s_full + 2;
@@ -91,13 +95,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y, b = blockIdx.z;
     const int D = p.n_head * HD;
-    const int q0 = blockIdx.x * 2 * QT;
-    const int row0 = b * p.n_ctx;
+    const int nkv = p.nkv;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 2);           // one commit from each MMA issuer
         for (int s = 0; s < NST; ++s) {
             mbar_init(kv_full + s, 1);
             mbar_init(kv_empty + s, 2);  // one commit from each MMA issuer
@@ -125,29 +128,49 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Persistent: this CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...  Every role walks
+    // the same item sequence; K/V tiles and per-tile steps are numbered across items, so the
+    // next item's Q and K/V loads and its first Q K^T overlap the end of the current item.
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_LOW));
       if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
-        uint32_t issued = 0, last_parity = 0;
-        mbar_arrive_expect_tx(q_full, 2 * Q_BYTES);
-        tma_load_2d(sQ, &tm, q_full, h * HD, row0 + q0);
-        tma_load_2d(sQ + Q_BYTES, &tm, q_full, h * HD, row0 + q0 + QT);
-        for (int j = 0; j < p.nkv; ++j) {
-            const int s = j % NST;
-            const uint32_t ph = (uint32_t)(j / NST) & 1u;
-            if (*abort_flag || !mbar_wait(kv_empty + s, ph ^ 1u, p.ctl)) {
+        uint32_t issued = 0, last_parity = 0, g = 0;
+        int k = 0;
+        for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++k) {
+            const int qb = item % p.n_qblk, bh = item / p.n_qblk;
+            const int h = bh % p.n_head, row0 = (bh / p.n_head) * p.n_ctx, q0 = qb * 2 * QT;
+            // Q of the previous item is no longer read once both issuers' last Q K^T completed
+            if (*abort_flag || (k > 0 && !mbar_wait(q_empty, (uint32_t)(k - 1) & 1u, p.ctl))) {
                 *abort_flag = 1;
                 break;
             }
-            uint8_t *k = sKV + s * 2 * KV_BYTES;
-            mbar_arrive_expect_tx(kv_full + s, 2 * KV_BYTES);
-            tma_load_2d(k, &tm, kv_full + s, D + h * HD, row0 + j * KT);
-            tma_load_2d(k + KV_BYTES, &tm, kv_full + s, 2 * D + h * HD, row0 + j * KT);
-            issued |= 1u << s;
-            last_parity = (last_parity & ~(1u << s)) | (ph << s);
+            mbar_arrive_expect_tx(q_full, 2 * Q_BYTES);
+            tma_load_2d(sQ, &tm, q_full, h * HD, row0 + q0);
+            tma_load_2d(sQ + Q_BYTES, &tm, q_full, h * HD, row0 + q0 + QT);
+            bool stop = false;
+            for (int j = 0; j < nkv; ++j, ++g) {
+                const int s = g % NST;
+                const uint32_t ph = (g / NST) & 1u;
+                if (*abort_flag || !mbar_wait(kv_empty + s, ph ^ 1u, p.ctl)) {
+                    *abort_flag = 1;
+                    stop = true;
+                    break;
+                }
+                uint8_t *kb = sKV + s * 2 * KV_BYTES;
+                mbar_arrive_expect_tx(kv_full + s, 2 * KV_BYTES);
+                tma_load_2d(kb, &tm, kv_full + s, D + h * HD, row0 + j * KT);
+                tma_load_2d(kb + KV_BYTES, &tm, kv_full + s, 2 * D + h * HD, row0 + j * KT);
+                issued |= 1u << s;
+                last_parity = (last_parity & ~(1u << s)) | (ph << s);
+            }
+            if (stop) {
+                ++k;  // this item's Q was issued
+                break;
+            }
         }
-        mbar_wait(q_full, 0, p.ctl);
+        // no copy of this CTA may still be in flight when it exits
+        if (k > 0) mbar_wait(q_full, (uint32_t)(k - 1) & 1u, p.ctl);
         for (int s = 0; s < NST; ++s)
             if ((issued >> s) & 1u) mbar_wait(kv_full + s, (last_parity >> s) & 1u, p.ctl);
     } else if ((warp == 1 || warp == 2) && lane == 0) {
@@ -160,37 +183,49 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
         constexpr uint32_t IDESC_O = idesc_bf16_f32(QT, HD) | (1u << 16);  // B (V) is MN-major
         const uint32_t sq = smem_u32(sQ) + t * Q_BYTES, skv = smem_u32(sKV);
         const uint32_t dS = tmem + 128u * t, dO = tmem + 256u + 64u * t, aP = tmem + 384u + 64u * t;
-        bool ok = mbar_wait(q_full, 0, p.ctl) && mbar_wait(kv_full, 0, p.ctl);
-        auto issue_s = [&](int s) {
+        auto issue_s = [&](uint32_t s) {
             const uint64_t a = sdesc_sw128(sq), bk = sdesc_sw128(skv + s * 2 * KV_BYTES);
 #pragma unroll
-            for (int k = 0; k < HD / 16; ++k)
-                umma_bf16(dS, a + (uint64_t)(2 * k), bk + (uint64_t)(2 * k), IDESC_S, k != 0);
+            for (int kk = 0; kk < HD / 16; ++kk)
+                umma_bf16(dS, a + (uint64_t)(2 * kk), bk + (uint64_t)(2 * kk), IDESC_S, kk != 0);
             umma_commit(s_full + t);
         };
-        if (ok) {
-            tc_fence_after();
-            issue_s(0);
-        }
-        for (int j = 0; ok && j < p.nkv; ++j) {
-            const int s = j % NST;
-            if (j + 1 < p.nkv) {
-                const int s1 = (j + 1) % NST;
-                ok = !*abort_flag && mbar_wait(kv_full + s1, (uint32_t)((j + 1) / NST) & 1u, p.ctl) &&
-                     mbar_wait(s_free + t, (uint32_t)j & 1u, p.ctl);
-                if (!ok) break;
-                tc_fence_after();
-                issue_s(s1);
-            }
-            ok = !*abort_flag && mbar_wait(p_full + t, (uint32_t)j & 1u, p.ctl);
+        bool ok = true;
+        uint32_t g = 0, G = 0;  // K/V tiles consumed, steps of this tile (both across items)
+        int k = 0;
+        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++k) {
+            // S_t(0) of this item: its Q has landed, K tile 0 has landed, and the softmax has
+            // read the previous item's last S_t.
+            ok = !*abort_flag && mbar_wait(q_full, (uint32_t)k & 1u, p.ctl) &&
+                 mbar_wait(kv_full + g % NST, (g / NST) & 1u, p.ctl) &&
+                 (G == 0 || mbar_wait(s_free + t, (G - 1) & 1u, p.ctl));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t vb = skv + s * 2 * KV_BYTES + KV_BYTES;
+            issue_s(g % NST);
+            if (nkv == 1) umma_commit(q_empty);
+            for (int j = 0; j < nkv; ++j) {
+                const uint32_t s = (g + j) % NST;
+                if (j + 1 < nkv) {
+                    const uint32_t g1 = g + j + 1;
+                    ok = !*abort_flag && mbar_wait(kv_full + g1 % NST, (g1 / NST) & 1u, p.ctl) &&
+                         mbar_wait(s_free + t, (G + j) & 1u, p.ctl);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(g1 % NST);
+                    if (j + 2 == nkv) umma_commit(q_empty);  // the item's last Q K^T
+                }
+                ok = !*abort_flag && mbar_wait(p_full + t, (G + j) & 1u, p.ctl);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t vb = skv + s * 2 * KV_BYTES + KV_BYTES;
 #pragma unroll
-            for (int k = 0; k < KT / 16; ++k)  // P (A operand) from TMEM: 16 keys = 8 columns
-                umma_bf16_tmem_a(dO, aP + 8u * k, sdesc_sw128_mn(vb + k * 2048), IDESC_O, (j | k) != 0);
-            umma_commit(o_full + t);
-            umma_commit(kv_empty + s);  // one of the two arrivals that free K/V stage s
+                for (int kk = 0; kk < KT / 16; ++kk)  // P (A operand) from TMEM: 16 keys = 8 columns
+                    umma_bf16_tmem_a(dO, aP + 8u * kk, sdesc_sw128_mn(vb + kk * 2048), IDESC_O, (j | kk) != 0);
+                umma_commit(o_full + t);
+                umma_commit(kv_empty + s);  // one of the two arrivals that free K/V stage s
+            }
+            g += nkv;
+            G += nkv;
         }
         if (!ok) *abort_flag = 1;
         umma_commit(drain + t);
@@ -209,112 +244,117 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
         const uint32_t tO = tmem + lane_off + 256u + 64u * t;
         const uint32_t tP = tmem + lane_off + 384u + 64u * t;
         const float sl2 = p.scale_log2;
-        float m = -INFINITY, l = 0.0f;
         bool ok = true;
-        if (t == 1 && lane == 0) mbar_arrive(turn);   // tile 0 takes the first turn
-        for (int j = 0; j < p.nkv; ++j) {
-            ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(s_full + t, (uint32_t)j & 1u, p.ctl));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sv[4][32];
+        uint32_t G = 0;                                        // steps of this tile across items
+        if (t == 1 && lane == 0) mbar_arrive(turn);            // tile 0 takes the first turn
+        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            const int qb = item % p.n_qblk, bh = item / p.n_qblk;
+            const int h = bh % p.n_head, row0 = (bh / p.n_head) * p.n_ctx, q0 = qb * 2 * QT;
+            const bool last_item = item + (int)gridDim.x >= p.n_items;
+            float m = -INFINITY, l = 0.0f;
+            for (int j = 0; j < nkv; ++j) {
+                const uint32_t par = (G + j) & 1u;
+                ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(s_full + t, par, p.ctl));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sv[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, sv[c]);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free + t);           // S_t may now be overwritten
-            const int kvalid = p.n_ctx - j * KT;               // keys of this tile inside the window
-            if (kvalid < KT) {
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, sv[c]);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free + t);           // S_t may now be overwritten
+                const int kvalid = p.n_ctx - j * KT;               // keys of this tile inside the window
+                if (kvalid < KT) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= kvalid) sv[c][i] = 0xff800000u;  // -inf
+                }
+                // row maximum: 8 independent partial maxima, then a tree (no 128-long chain)
+                float pm[8];
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) pm[kk] = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (32 * c + i >= kvalid) sv[c][i] = 0xff800000u;  // -inf
-            }
-            // row maximum: 8 independent partial maxima, then a tree (no 128-long chain)
-            float pm[8];
+                    for (int i = 0; i < 32; i += 2)
+                        pm[(i >> 1) & 7] = max3(pm[(i >> 1) & 7], __uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1]));
+                const float mx = max3(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+                const float m_new = fmaxf(m, mx);
+                if (j == 0) {
+                    m = m_new;
+                } else {
+                    // PV of the previous tile is done: O is stable and the P buffer is free.
+                    ok = __all_sync(0xffffffffu, mbar_wait(o_full + t, par ^ 1u, p.ctl));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const bool need = (m_new - m) * sl2 > 8.0f;
+                    if (__any_sync(0xffffffffu, need)) {
+                        float f = 1.0f;
+                        if (need) {
+                            f = ex2((m - m_new) * sl2);
+                            l *= f;
+                            m = m_new;
+                        }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) pm[k] = -INFINITY;
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t v[32];
+                            tmem_ld32(tO + 32u * half, v);
+                            tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; i += 2)
-                    pm[(i >> 1) & 7] = max3(pm[(i >> 1) & 7], __uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1]));
-            const float mx = max3(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-            const float m_new = fmaxf(m, mx);
-            if (j == 0) {
-                m = m_new;
-            } else {
-                // PV of the previous tile is done: O is stable and the P buffer is free.
-                ok = __all_sync(0xffffffffu, mbar_wait(o_full + t, (uint32_t)(j - 1) & 1u, p.ctl));
+                            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                            tmem_st32(tO + 32u * half, v);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                // Ping-pong: the two tiles take turns in the exponential section, so one tile's
+                // S load, row maximum and waits overlap the other tile's exponentials.
+                ok = __all_sync(0xffffffffu, mbar_wait(turn + t, par, p.ctl));
                 if (!ok) break;
-                tc_fence_after();
-                const bool need = (m_new - m) * sl2 > 8.0f;
-                if (__any_sync(0xffffffffu, need)) {
-                    float f = 1.0f;
-                    if (need) {
-                        f = ex2((m - m_new) * sl2);
-                        l *= f;
-                        m = m_new;
-                    }
+                const float mc = m * sl2;
+                // exponentials: scale-and-subtract and the row sum two lanes at a time (packed fp32)
+                const uint64_t sl2x2 = f2_pack(sl2, sl2), nmcx2 = f2_pack(-mc, -mc);
+                uint64_t ps[4];                                    // 4 x 2 independent partial sums
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t v[32];
-                        tmem_ld32(tO + 32u * half, v);
-                        tmem_wait_ld();
+                for (int kk = 0; kk < 4; ++kk) ps[kk] = 0ull;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-                        tmem_st32(tO + 32u * half, v);
+                for (int hh = 0; hh < 2; ++hh) {                   // 64 keys -> 32 packed bf16 pairs
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * hh + cc;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const uint64_t x = fma_f2(f2_pack(__uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1])),
+                                                      sl2x2, nmcx2);
+                            float x0, x1;
+                            f2_unpack(x, x0, x1);
+                            const float e0 = ex2(x0), e1 = ex2(x1);
+                            ps[(i >> 1) & 3] = add_f2(ps[(i >> 1) & 3], f2_pack(e0, e1));
+                            pk[16 * cc + (i >> 1)] = pack_bf16(e0, e1);
+                        }
                     }
-                    tmem_wait_st();
+                    tmem_st32(tP + 32u * hh, pk);
                 }
+                __syncwarp();
+                // tile 1's very last step is the CTA's last turn
+                if (lane == 0 && (t == 0 || !(last_item && j + 1 == nkv))) mbar_arrive(turn + (1 - t));
+                tmem_wait_st();
+                {
+                    const uint64_t s2 = add_f2(add_f2(ps[0], ps[1]), add_f2(ps[2], ps[3]));
+                    float a0, a1;
+                    f2_unpack(s2, a0, a1);
+                    l += a0 + a1;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full + t);
             }
-            // Ping-pong: the two tiles take turns in the exponential section, so one tile's
-            // S load, row maximum and waits overlap the other tile's exponentials.
-            ok = __all_sync(0xffffffffu, mbar_wait(turn + t, (uint32_t)j & 1u, p.ctl));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full + t, (G + nkv - 1) & 1u, p.ctl));
             if (!ok) break;
-            const float mc = m * sl2;
-            // exponentials: scale-and-subtract and the row sum two lanes at a time (packed fp32)
-            const uint64_t sl2x2 = f2_pack(sl2, sl2), nmcx2 = f2_pack(-mc, -mc);
-            uint64_t ps[4];                                    // 4 x 2 independent partial sums
-#pragma unroll
-            for (int k = 0; k < 4; ++k) ps[k] = 0ull;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {                   // 64 keys -> 32 packed bf16 pairs
-                uint32_t pk[32];
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c = 2 * hh + cc;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const uint64_t x = fma_f2(f2_pack(__uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1])),
-                                                  sl2x2, nmcx2);
-                        float x0, x1;
-                        f2_unpack(x, x0, x1);
-                        const float e0 = ex2(x0), e1 = ex2(x1);
-                        ps[(i >> 1) & 3] = add_f2(ps[(i >> 1) & 3], f2_pack(e0, e1));
-                        pk[16 * cc + (i >> 1)] = pack_bf16(e0, e1);
-                    }
-                }
-                tmem_st32(tP + 32u * hh, pk);
-            }
-            __syncwarp();
-            if (lane == 0 && (t == 0 || j + 1 < p.nkv)) mbar_arrive(turn + (1 - t));  // other tile's turn
-            tmem_wait_st();
-            {
-                const uint64_t s2 = add_f2(add_f2(ps[0], ps[1]), add_f2(ps[2], ps[3]));
-                float a0, a1;
-                f2_unpack(s2, a0, a1);
-                l += a0 + a1;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + t);
-        }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full + t, (uint32_t)(p.nkv - 1) & 1u, p.ctl));
-        if (!ok) {
-            *abort_flag = 1;
-        } else {
             tc_fence_after();
             const float inv = 1.0f / l;
             const int q = q0 + t * QT + r;
@@ -329,14 +369,18 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
                     for (int c = 0; c < 4; ++c) {
                         uint32_t w[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            w[k] = pack_bf16(__uint_as_float(v[8 * c + 2 * k]) * inv,
-                                             __uint_as_float(v[8 * c + 2 * k + 1]) * inv);
+                        for (int kk = 0; kk < 4; ++kk)
+                            w[kk] = pack_bf16(__uint_as_float(v[8 * c + 2 * kk]) * inv,
+                                              __uint_as_float(v[8 * c + 2 * kk + 1]) * inv);
                         dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
+            // O has been read: the next item's first P V may overwrite it (its p_full follows)
+            tc_fence_before();
+            G += nkv;
         }
+        if (!ok) *abort_flag = 1;
     }
     tc_fence_before();
     __syncthreads();
@@ -356,7 +400,7 @@ int attention_prepare() {
 }
 
 int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
-                     cudaStream_t s) {
+                     int num_sms, cudaStream_t s) {
     if (batch <= 0) return WH_OK;
     const int D = n_head * HD;
     CUtensorMap tm;
@@ -365,10 +409,15 @@ int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *ou
     a.n_ctx = n_ctx;
     a.n_head = n_head;
     a.nkv = (n_ctx + KT - 1) / KT;
+    a.n_qblk = (n_ctx + 2 * QT - 1) / (2 * QT);
+    const long long items = (long long)a.n_qblk * n_head * batch;
+    if (items > (1LL << 30)) return WH_EINVAL;
+    a.n_items = (int)items;
     a.out = reinterpret_cast<__nv_bfloat16 *>(out);
     a.scale_log2 = 0.125f * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
     a.ctl = ctl;
-    dim3 grid((n_ctx + 2 * QT - 1) / (2 * QT), n_head, batch);
+    // one CTA per SM (shared memory and TMEM allow no second), persistent over the items
+    const int grid = a.n_items < num_sms ? a.n_items : num_sms;
     k_attention_tc<<<grid, THREADS, SMEM_BYTES, s>>>(tm, a);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;

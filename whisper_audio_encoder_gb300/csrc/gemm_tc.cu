@@ -7,14 +7,17 @@
 //   conv1 + GELU written straight into conv2's im2col matrix, conv2 + GELU + stored positions
 //   (model.nu: conv1 -> GELU -> conv2 -> GELU, embed_positions added).
 //
-// Kernel structure (one CTA per SM, persistent over output tiles of 128 x BN):
-//   warp 0      one thread issues TMA loads of A/B k-blocks (64 wide, 128-byte swizzle) into
-//               a STAGES-deep shared-memory ring (full/empty mbarriers)
-//   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, N=BN, K=16) into one of
-//               two TMEM accumulators and commits stage releases / accumulator-ready barriers
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (each warp owns one 32-lane quarter of
-//               TMEM = 32 rows), apply bias / GELU / residual / positions, store to global;
-//               then release the accumulator so the MMA of tile i+2 can start.
+// Kernel structure: persistent CTA pairs (a cluster of two CTAs on two SMs, cta_group::2),
+// each pair walking 256 x BN output tiles (BN = 256, or 128 when a segment is not a multiple
+// of 256), k-blocks 64 wide:
+//   warp 0      (both CTAs) one thread issues TMA loads of this CTA's 128 rows of A and BN/2
+//               rows of B (128-byte swizzle) into a STAGES-deep shared-memory ring
+//   warp 1      allocates TMEM in both CTAs; on the even CTA one thread issues tcgen05.mma
+//               (M=256, N=BN, K=16) reading both CTAs' operand halves, into one of two TMEM
+//               accumulators, and multicasts its commits to both CTAs
+//   warps 2..9  (both CTAs) epilogue on this CTA's 128 rows: tcgen05.ld, bias / GELU /
+//               residual / positions, TMA store through a per-warp staging tile; then hand
+//               the accumulator back so the MMA of tile i+2 can start.
 // Every wait is bounded (DevCtl::wait_ns); on expiry the block records WH_ETIMEOUT, winds
 // down, waits for its own copies and MMAs in flight, frees TMEM and returns.
 #include "common.cuh"

@@ -48,7 +48,7 @@ int frontend_launch(const float *pcm, int64_t n, int batch, int n_mels, float *m
 int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,
                      cudaStream_t s);
 int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
-                     cudaStream_t s);
+                     int num_sms, cudaStream_t s);
 int attention_prepare();
 int stem_im2col_launch(const float *mel, int batch, int n_mels, void *a1, cudaStream_t s);
 int pack_conv_weight_launch(const void *w, int c_out, int c_in, void *wp, cudaStream_t s);

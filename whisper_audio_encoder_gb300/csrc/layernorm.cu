@@ -13,23 +13,27 @@ namespace {
 constexpr int LN_THREADS = 256;
 constexpr int MAXV = 16;  // float4 per lane: d <= 2048
 
-// d a multiple of 128: each lane holds d / 128 float4 (16-byte loads and stores).
-template <bool OUT_BF16>
+// d a multiple of 128: each lane holds d / 128 float4 (16-byte loads and stores).  NV > 0
+// fixes d = 128 NV at compile time (registers sized to the row: more rows in flight per SM);
+// NV = 0 takes d at run time (up to MAXV float4 per lane).
+template <int NV, bool OUT_BF16>
 __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restrict__ x, int rows, int d,
                                                           const float *__restrict__ g,
                                                           const float *__restrict__ b, void *__restrict__ y) {
+    constexpr int CAP = NV > 0 ? NV : MAXV;
     const int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const int nv = d >> 7;
+    const int nv = NV > 0 ? NV : d >> 7;
+    if (NV > 0) d = NV * 128;
     const float4 *xr = reinterpret_cast<const float4 *>(x + (long long)row * d);
-    float4 v[MAXV];
+    float4 v[CAP];
     float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i)
+    for (int i = 0; i < CAP; ++i)
         if (i < nv) v[i] = __ldg(xr + i * 32 + lane);
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i)
+    for (int i = 0; i < CAP; ++i)
         if (i < nv) {
             s0 += v[i].x + v[i].y;
             s1 += v[i].z + v[i].w;
@@ -37,7 +41,7 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restric
     const float mean = warp_sum(s0 + s1) / (float)d;
     float q0 = 0.0f, q1 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i)
+    for (int i = 0; i < CAP; ++i)
         if (i < nv) {
             const float a = v[i].x - mean, bb = v[i].y - mean, c = v[i].z - mean, e = v[i].w - mean;
             q0 = fmaf(a, a, fmaf(bb, bb, q0));
@@ -47,7 +51,7 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restric
     const float4 *g4 = reinterpret_cast<const float4 *>(g);
     const float4 *b4 = reinterpret_cast<const float4 *>(b);
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i)
+    for (int i = 0; i < CAP; ++i)
         if (i < nv) {
             const int c = i * 32 + lane;
             const float4 gg = __ldg(g4 + c), bb = __ldg(b4 + c);
@@ -61,6 +65,15 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restric
                 reinterpret_cast<float4 *>(y)[(long long)row * (d >> 2) + c] = make_float4(o0, o1, o2, o3);
             }
         }
+}
+
+template <int NV>
+void launch_ln(int grid, cudaStream_t s, const float *x, int rows, int d, const float *g, const float *b, void *y,
+               int y_bf16) {
+    if (y_bf16)
+        k_layernorm<NV, true><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+    else
+        k_layernorm<NV, false><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
 }
 
 // d a multiple of 64 but not of 128: float2 per lane.
@@ -115,10 +128,14 @@ int layernorm_launch(const float *x, int rows, int d, const float *g, const floa
     if (d % 64 != 0 || d < 64 || d > 128 * MAXV) return WH_EINVAL;
     const int grid = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
     if (d % 128 == 0) {
-        if (y_bf16)
-            k_layernorm<true><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
-        else
-            k_layernorm<false><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+        switch (d / 128) {  // the family's widths (384, 512, 768, 1024, 1280) get exact registers
+            case 3: launch_ln<3>(grid, s, x, rows, d, g, b, y, y_bf16); break;
+            case 4: launch_ln<4>(grid, s, x, rows, d, g, b, y, y_bf16); break;
+            case 6: launch_ln<6>(grid, s, x, rows, d, g, b, y, y_bf16); break;
+            case 8: launch_ln<8>(grid, s, x, rows, d, g, b, y, y_bf16); break;
+            case 10: launch_ln<10>(grid, s, x, rows, d, g, b, y, y_bf16); break;
+            default: launch_ln<0>(grid, s, x, rows, d, g, b, y, y_bf16); break;
+        }
     } else {
         if (y_bf16)
             k_layernorm64<true><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);

@@ -304,7 +304,7 @@ int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weight
             if ((rc = run_gemm(g, GEMM_BF16, st, s, TR_GEMM_QKV))) return rc;
         }
         trace_begin(TR_ATTN, s);
-        if ((rc = attention_launch(qkv, batch, N_CTX, H, ao, ctl_of(st), s))) return rc;
+        if ((rc = attention_launch(qkv, batch, N_CTX, H, ao, ctl_of(st), st->num_sms, s))) return rc;
         trace_end(TR_ATTN, s, 4.0 * batch * (double)N_CTX * N_CTX * d, (double)rows * d * 8.0);
         if ((rc = run_gemm(gemm(ao, d, rows, d, Lw.wo, d, d, Lw.bo, x, d), GEMM_RESID_F32, st, s, TR_GEMM_OUT)))
             return rc;
@@ -358,7 +358,7 @@ int wh_attention(const wh_bf16 *qkv, int batch, int n_ctx, int n_head, wh_bf16 *
     if (int rc = ensure_device(&st)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     trace_begin(TR_ATTN, s);
-    const int rc = attention_launch(qkv, batch, n_ctx, n_head, out, ctl_of(st), s);
+    const int rc = attention_launch(qkv, batch, n_ctx, n_head, out, ctl_of(st), st->num_sms, s);
     trace_end(TR_ATTN, s, 4.0 * batch * (double)n_ctx * n_ctx * 64 * n_head, (double)batch * n_ctx * n_head * 64 * 8.0);
     return rc;
 }
