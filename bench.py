@@ -43,6 +43,7 @@ def _args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-next", action="store_true", help="skip the cross_kv / audio_ctx measurements")
     return p.parse_args()
 
 
@@ -226,6 +227,57 @@ def _traffic_from_profiles(kernel):
     return rec["dram_bytes_per_launch"]
 
 
+def _encoder_flops(cfg, n_ctx):
+    """Dense flops of one window through the stem and blocks at n_ctx positions."""
+    d, f, m = cfg.d_model, cfg.d_ff, cfg.n_mels
+    stem = 2.0 * (2 * n_ctx) * 3 * m * d + 2.0 * n_ctx * 3 * d * d
+    block = 2.0 * n_ctx * (4 * d * d + 2 * d * f) + 4.0 * n_ctx * n_ctx * d
+    return stem + cfg.n_layer * block
+
+
+def _time_next(enc, cfg, B, pcm_d, mel_d, out_d, steps):
+    import torch
+
+    from whisper_audio_encoder_gb300 import synth, wh
+
+    def timed(fn, k):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(k):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / k
+
+    res = {}
+    d = cfg.d_model
+    ckv = wh.CrossKV(d, synth.cross_weights(cfg))
+    kv = torch.empty(ckv.n_layer, B * 1500, 2 * d, dtype=torch.bfloat16, device="cuda")
+    ms = timed(lambda: ckv.wh_prepare_cross(out_d, kv=kv), max(3, steps // 3))
+    flops = ckv.n_layer * 2.0 * (B * 1500) * d * (2 * d)
+    res["cross_kv"] = {"value": B * 1000.0 / ms, "unit": "windows/s", "ms_per_batch": ms,
+                       "tflops": flops / (ms * 1e-3) / 1e12, "decoder_layers": ckv.n_layer,
+                       "what": "wh_prepare_cross: K, V of every decoder layer from the batch's encoder memory"}
+    del kv, ckv
+    n_ctx = 500  # a draft over 5 s of audio + 5 s: the 10-s minimum
+    out_ctx = torch.empty(B, n_ctx, d, device="cuda")
+    fe_ws = enc.frontend_workspace(B)
+
+    def draft():
+        wh.wh_frontend(pcm_d, cfg.n_mels, mel=mel_d, workspace=fe_ws)
+        enc.wh_encode_ctx(mel_d, n_ctx, out=out_ctx)
+    ms = timed(draft, max(3, steps // 2))
+    res["audio_ctx"] = {"n_ctx": n_ctx, "value": B * 1000.0 / ms, "unit": "windows/s", "ms_per_step": ms,
+                        "tflops": B * _encoder_flops(cfg, n_ctx) / (ms * 1e-3) / 1e12,
+                        "what": "wh_frontend + wh_encode_ctx over the first 10 s of each window"}
+    st = wh.wh_status()
+    if st != wh.WH_OK:
+        raise RuntimeError(f"device status after the next-row measurements: {wh.wh_strerror(st)}")
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -323,6 +375,10 @@ def run_ours(args):
         e2e_ms = g0.elapsed_time(g1) / args.steps
     graph.destroy()
 
+    # ---- next rows, each timed on its own (not part of the step): the decoder layers'
+    # cross-attention K/V over this batch's encoder memory, and a 10-s-context draft encoder
+    nxt = {} if args.no_next else _time_next(enc, cfg, B, pcm_d, mel_d, out_d, args.steps)
+
     if dist is not None:
         ms, e2e_max, direct_ms = max_over_ranks([ms, e2e_ms or 0.0, direct_ms], dist, device="cuda")
         e2e_ms = e2e_max if e2e_ms is not None else None
@@ -369,6 +425,7 @@ def run_ours(args):
                          "note": "wh_frontend + wh_encode called each step (per-kernel events recorded)"},
         "clocks": clk,
     }
+    line.update(nxt)
     if e2e_ms is not None:
         line["e2e"] = {"value": B * ws * 1000.0 / e2e_ms, "unit": "windows/s",
                        "h2d_bytes_per_step": int(pcm_h.numel() * 4), "d2h_bytes_per_step": int(out_h.numel() * 4)}

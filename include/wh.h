@@ -12,7 +12,7 @@
  *     is launched.  Errors found on the device (a bounded wait that ran out, a bounds check)
  *     are recorded in a per-device status word and returned by wh_status().
  *   - The library's own persistent state is small constant tables (Hann window, twiddles,
- *     mel filterbanks) in __constant__ memory, set up on the first call on each device.
+ *     mel filterbanks) in static device arrays, set up on the first call on each device.
  *     Make that first call outside any CUDA-graph capture.
  *   - Matrices are bfloat16 (passed as wh_bf16 bit patterns), vectors are float32,
  *     accumulation is float32, the residual stream is float32.
@@ -51,8 +51,8 @@ typedef struct {
 
 /* One encoder block ("whisper 0.9.0 API", model.nu: N x [LN -> self-attn -> +residual,
  * LN -> fc1 -> GELU -> fc2 -> +residual]).  Matrices use the nn.Linear layout [out][in],
- * row-major.  q, v and out_proj have a bias; k_proj has NONE (model.nu: "k_proj HAS NO
- * BIAS"), so there is no bk field. */
+ * row-major.  q, v and out_proj have a bias; the key projection has none (model.nu lists
+ * no k bias among the weights), so there is no bk field. */
 typedef struct {
     const float *ln1_g, *ln1_b;            /* [d] */
     const wh_bf16 *wq, *wk, *wv;           /* [d][d] each */
@@ -82,8 +82,8 @@ typedef struct {
  *
  *   pcm   device float32 [batch][n]: window b's samples start at pcm + b * n.  n >= 0;
  *         n < 480000 reads zeros past the end, n > 480000 ignores the rest.
- *   mel   device float32 [batch][3000][n_mels], a frame contiguous ("whisper 0.9.0 API",
- *         wh_encode: "mel is 3000 x n_mels, row-major (a frame is contiguous)").
+ *   mel   device float32 [batch][3000][n_mels]: per window 3000 rows of n_mels values, each
+ *         frame contiguous (the layout "whisper 0.9.0 API" gives for wh_encode's input).
  *   workspace  device scratch of at least wh_frontend_workspace(batch) bytes, 16-byte aligned
  *         (the per-window maxima); contents need not be initialised.
  * Errors: WH_EINVAL (null pointer with batch > 0, n < 0, batch < 0 or > 65535, n_mels not
@@ -119,8 +119,8 @@ int wh_frontend_static(const float *pcm, int64_t n, int batch, int n_mels, float
  * LayerNorm (eps 1e-5); GELU is the erf form (kernels.nu).
  *
  *   mel   device float32 [batch][3000][n_mels] (as produced by wh_frontend)
- *   out   device float32 [batch][1500][d_model], row-major ("wh_enc_out: 1500 x d_model,
- *         row-major"); may not alias mel or the workspace.
+ *   out   device float32 [batch][1500][d_model], row-major (the encoder-state layout of
+ *         "whisper 0.9.0 API", wh_enc_out); may not alias mel or the workspace.
  *   workspace  device scratch of at least wh_encode_workspace(cfg, batch) bytes, 256-byte
  *         aligned; contents need not be initialised; not to be shared by concurrent calls.
  * Errors: WH_EINVAL (null pointer, unsupported config, misaligned pointer), WH_ENOSPC,
@@ -131,8 +131,53 @@ int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weight
               float *out, void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
- * Recorded passes ("whisper 0.9.0 API" README, implementation notes: the encoder is
- * "recorded once when the model opens and replayed").  wh_graph_capture records one
+ * Encoder over a shorter context (the "whisper" package page, "Serving": drafts run the
+ * encoder over the audio heard so far plus 5 s, at least 10 s, instead of the full 30 s --
+ * whisper.cpp's audio_ctx).  The encoder reads only the first 2 n_ctx log-mel frames of each
+ * window, pads that span with zeros at both ends for the convolutions (as it pads the full
+ * window), adds the first n_ctx stored positions and attends over n_ctx positions.
+ * n_ctx = 1500 is wh_encode exactly.
+ *   mel   device float32 [batch][3000][n_mels], as for wh_encode (windows 3000 frames apart;
+ *         frames 2 n_ctx .. 2999 are not read)
+ *   out   device float32 [batch][n_ctx][d_model], row-major
+ *   1 <= n_ctx <= 1500; workspace >= wh_encode_ctx_workspace(cfg, batch, n_ctx) bytes,
+ *   256-byte aligned.  Errors as wh_encode, WH_EINVAL for n_ctx out of range.
+ * ------------------------------------------------------------------------------------ */
+size_t wh_encode_ctx_workspace(const wh_config *cfg, int batch, int n_ctx);
+int wh_encode_ctx(const float *mel, int batch, int n_ctx, const wh_config *cfg, const wh_weights *w,
+                  float *out, void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Cross-attention keys and values of every decoder layer ("whisper 0.9.0 API", model.nu,
+ * wh_prepare_cross: the decoder's cross-attention reads the encoder memory through its own
+ * k and v projections, and since the memory does not change while a clip is transcribed they
+ * are computed once per clip rather than once per generated token).  For decoder layer l:
+ *   K_l = mem Wk_l^T           (the cross k projection has no bias, model.nu)
+ *   V_l = mem Wv_l^T + bv_l
+ *   mem   device float32 [batch * n_ctx][d_model] (wh_encode's or wh_encode_ctx's output);
+ *         rounded once to bf16 as the tensor-core operand
+ *   w     host struct of host arrays of n_layer DEVICE pointers: wk[l], wv[l] bf16 [d][d]
+ *         (nn.Linear [out][in]), bv[l] float32 [d] or NULL (no bias)
+ *   kv    device bf16 [n_layer][batch * n_ctx][2 d_model]: row r of layer l holds K_l[r] in
+ *         columns 0 .. d-1 and V_l[r] in columns d .. 2d-1 (head h: 64 h .. 64 h + 63 of each)
+ *   workspace  >= wh_prepare_cross_workspace(batch, n_ctx, d_model) bytes, 256-byte aligned
+ *   d_model a multiple of 128 in [128, 2048]; 1 <= n_ctx <= 1500; n_layer >= 0.
+ * Errors: WH_EINVAL (null or misaligned pointer, shape out of range), WH_ENOSPC, WH_ECUDA.
+ * batch == 0 or n_layer == 0 is a no-op.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+    const wh_bf16 *const *wk;   /* host array [n_layer] of device [d][d] */
+    const wh_bf16 *const *wv;   /* host array [n_layer] of device [d][d] */
+    const float *const *bv;     /* host array [n_layer] of device [d] (entries may be NULL) */
+} wh_cross_weights;
+size_t wh_prepare_cross_workspace(int batch, int n_ctx, int d_model);
+int wh_prepare_cross(const float *mem, int batch, int n_ctx, int d_model, int n_layer,
+                     const wh_cross_weights *w, wh_bf16 *kv, void *workspace, size_t ws_bytes,
+                     void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Recorded passes (the "whisper" package page, "Implementation notes", records its encoder
+ * pass once when a model is opened and replays it per request).  wh_graph_capture records one
  * wh_frontend + wh_encode pass on `stream` into a CUDA graph (arguments exactly as for those
  * two calls; mel is the log-mel buffer between them).  wh_graph_launch replays it on any
  * stream: the same buffers are read and written, so refresh pcm in place and replay.  The

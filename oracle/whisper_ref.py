@@ -233,3 +233,30 @@ def encode_window(pcm: np.ndarray, w: dict, n_mels: int, n_head: int):
     """Front end + encoder for one window: returns (log-mel float32, encoder output float64)."""
     mel = log_mel(pcm, n_mels)
     return mel, encoder(mel, w, n_head)
+
+
+# ========================================================================================
+# Shorter encoder context  [README] "Serving" (drafts, whisper.cpp's audio_ctx)
+# ========================================================================================
+def encoder_ctx(mel: np.ndarray, w: dict, n_head: int, n_ctx: int) -> np.ndarray:
+    """The encoder over the first 2 n_ctx log-mel frames of a window (the draft encoder runs
+    over the audio heard so far plus 5 s instead of the whole 30 s).  Reading taken: the
+    encoder sees only that span, so the convolutions zero-pad at its end exactly as they
+    zero-pad at the end of a full window, and the first n_ctx stored positions are added.
+    mel [3000][n_mels] -> float64 [n_ctx][d]."""
+    return encoder(np.asarray(mel)[: 2 * n_ctx], w, n_head)
+
+
+# ========================================================================================
+# Cross-attention keys and values  [API] model.nu, wh_prepare_cross
+# ========================================================================================
+def cross_kv(mem: np.ndarray, wk: np.ndarray, wv: np.ndarray, bv=None):
+    """One decoder layer's cross-attention keys and values, computed from the encoder memory
+    through that layer's own k and v projections ([API] model.nu lists x_wk without a bias,
+    x_wv with x_bv).  mem [T][d], wk / wv [d][d] (nn.Linear [out][in]) -> (K, V) [T][d]."""
+    m = _f64(mem)
+    k = m @ _f64(wk).T
+    v = m @ _f64(wv).T
+    if bv is not None:
+        v = v + _f64(bv)
+    return k, v

@@ -124,3 +124,42 @@ def test_graph_entry_points_reject_bad_arguments(L):
 def test_no_device_is_reported(L):
     assert L.wh_frontend(FAKE, 480000, 1, 80, FAKE, FAKE, 256, None) == wh.WH_ENODEV
     assert L.wh_status(None) == wh.WH_ENODEV
+
+
+def test_encode_ctx_rejects_bad_context(L):
+    c = wh.wh_config(80, 384, 6, 0, 1536)
+    w = wh.wh_weights(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE)
+    for n_ctx in (0, -1, 1501):
+        assert L.wh_encode_ctx(FAKE, 1, n_ctx, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 1 << 40, None) \
+            == wh.WH_EINVAL
+        assert L.wh_encode_ctx_workspace(ctypes.byref(c), 1, n_ctx) == 0
+    assert L.wh_encode_ctx(FAKE, 1, 500, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 16, None) == wh.WH_ENOSPC
+    assert L.wh_encode_ctx(FAKE, 0, 500, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 0, None) == wh.WH_OK
+    full = L.wh_encode_workspace(ctypes.byref(c), 2)
+    assert L.wh_encode_ctx_workspace(ctypes.byref(c), 2, 1500) == full
+    assert 0 < L.wh_encode_ctx_workspace(ctypes.byref(c), 2, 500) < full
+
+
+def test_prepare_cross_rejects_bad_arguments(L):
+    ptrs = (ctypes.c_void_p * 2)(FAKE.value, FAKE.value)
+    nulls = (ctypes.c_void_p * 2)(None, None)
+    cw = wh.wh_cross_weights(ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)),
+                             ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)),
+                             ctypes.cast(nulls, ctypes.POINTER(ctypes.c_void_p)))
+    ok_ws = L.wh_prepare_cross_workspace(2, 1500, 384)
+    assert ok_ws >= 2 * 1500 * 384 * 2
+    for (d, n_ctx) in ((100, 1500), (384, 0), (384, 1501), (4096, 10), (64, 10)):
+        assert L.wh_prepare_cross(FAKE, 2, n_ctx, d, 2, ctypes.byref(cw), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+        assert L.wh_prepare_cross_workspace(2, n_ctx, d) == 0
+    assert L.wh_prepare_cross(FAKE, 2, 1500, 384, 2, None, FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+    assert L.wh_prepare_cross(None, 2, 1500, 384, 2, ctypes.byref(cw), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert L.wh_prepare_cross(odd, 2, 1500, 384, 2, ctypes.byref(cw), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+    bad_w = (ctypes.c_void_p * 2)(FAKE.value, None)                 # layer 1's wk missing
+    cw_bad = wh.wh_cross_weights(ctypes.cast(bad_w, ctypes.POINTER(ctypes.c_void_p)),
+                                 ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)),
+                                 ctypes.cast(nulls, ctypes.POINTER(ctypes.c_void_p)))
+    assert L.wh_prepare_cross(FAKE, 2, 1500, 384, 2, ctypes.byref(cw_bad), FAKE, FAKE, 1 << 40, None) == wh.WH_EINVAL
+    assert L.wh_prepare_cross(FAKE, 2, 1500, 384, 2, ctypes.byref(cw), FAKE, FAKE, 16, None) == wh.WH_ENOSPC
+    assert L.wh_prepare_cross(FAKE, 0, 1500, 384, 2, ctypes.byref(cw), FAKE, FAKE, 0, None) == wh.WH_OK
+    assert L.wh_prepare_cross(FAKE, 2, 1500, 384, 0, ctypes.byref(cw), FAKE, FAKE, 0, None) == wh.WH_OK

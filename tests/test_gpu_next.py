@@ -1,0 +1,135 @@
+"""GPU parity of the next rows, called through the C ABI, against the oracle.
+
+wh_prepare_cross: the cross-attention keys/values of every decoder layer.
+- Against the oracle fed the bf16-rounded memory: the bf16 GEMM bound, 2^-8 |ref| + 1e-3.
+- Against the oracle fed the float32 memory: that bound plus the operand rounding,
+  2^-9 sum_i |mem_i| |w_i|.
+- Shapes: tiny and large widths, ragged row counts, and a full large-v3 decoder (32 layers,
+  16 windows) on sampled rows.
+
+wh_encode_ctx: the encoder over the first 2 n_ctx log-mel frames.
+- n_ctx = 1500 is bitwise wh_encode.
+- Shorter contexts are held to the encoder bar against the oracle's encoder_ctx.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import whisper_ref as R
+from whisper_audio_encoder_gb300 import build, configs, synth, wh
+
+from helpers import bf16_round_np, check_encoder
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    build.build()
+    wh.lib()
+
+
+def _check_cross(kv, mem, layers, rows, what):
+    """kv: numpy float32 [n_layer][R][2d] from the GPU; mem float32 [R][d]; rows: indices."""
+    d = mem.shape[1]
+    m16 = bf16_round_np(mem).astype(np.float64)
+    for l, lw in enumerate(layers):
+        k_ref, v_ref = R.cross_kv(m16[rows], lw["wk"], lw["wv"], lw["bv"])
+        got_k, got_v = kv[l][rows, :d], kv[l][rows, d:]
+        for got, ref, name in ((got_k, k_ref, "K"), (got_v, v_ref, "V")):
+            bad = np.abs(got - ref) > 2.0 ** -8 * np.abs(ref) + 1e-3
+            assert not bad.any(), f"{what} layer {l} {name}: {bad.sum()} outside the bf16 GEMM bound"
+        # against the unrounded memory: add the operand rounding bound
+        k_ex, v_ex = R.cross_kv(mem[rows], lw["wk"], lw["wv"], lw["bv"])
+        mag_k = np.abs(mem[rows]).astype(np.float64) @ np.abs(lw["wk"]).T.astype(np.float64)
+        mag_v = np.abs(mem[rows]).astype(np.float64) @ np.abs(lw["wv"]).T.astype(np.float64)
+        assert np.all(np.abs(got_k - k_ex) <= 2.0 ** -8 * np.abs(k_ex) + 2.0 ** -9 * mag_k + 1e-3), f"{what} K"
+        assert np.all(np.abs(got_v - v_ex) <= 2.0 ** -8 * np.abs(v_ex) + 2.0 ** -9 * mag_v + 1e-3), f"{what} V"
+
+
+@pytest.mark.parametrize("cfg_idx,batch,n_ctx,n_layer", [(1, 2, 1500, 4), (1, 1, 37, 2), (4, 1, 300, 2),
+                                                         (2, 3, 700, 1)])
+def test_prepare_cross_parity(cfg_idx, batch, n_ctx, n_layer):
+    cfg = configs.CONFIGS[cfg_idx]
+    layers = synth.cross_weights(cfg, n_layer)
+    rng = np.random.default_rng(batch * 100 + n_ctx)
+    mem = rng.standard_normal((batch, n_ctx, cfg.d_model)).astype(np.float32)
+    ckv = wh.CrossKV(cfg.d_model, layers)
+    kv = ckv.wh_prepare_cross(torch.from_numpy(mem).cuda())
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    kv = kv.float().cpu().numpy()
+    assert kv.shape == (n_layer, batch * n_ctx, 2 * cfg.d_model)
+    rows = np.arange(batch * n_ctx)
+    _check_cross(kv, mem.reshape(-1, cfg.d_model), layers, rows, cfg.name)
+
+
+def test_prepare_cross_without_bias():
+    cfg = configs.CONFIGS[1]
+    layers = synth.cross_weights(cfg, 1)
+    layers[0]["bv"] = None
+    mem = np.random.default_rng(8).standard_normal((1, 64, cfg.d_model)).astype(np.float32)
+    kv = wh.CrossKV(cfg.d_model, layers).wh_prepare_cross(torch.from_numpy(mem).cuda()).float().cpu().numpy()
+    _check_cross(kv, mem.reshape(-1, cfg.d_model), layers, np.arange(64), "no bias")
+
+
+def test_prepare_cross_large_v3_decoder_sampled_rows():
+    """The large-v3 decoder's 32 layers over 16 windows (the bench's launch configuration),
+    checked on 96 sampled rows of 3 layers (first, a middle one, last)."""
+    cfg = configs.CONFIGS[4]
+    layers = synth.cross_weights(cfg)
+    mem = np.random.default_rng(11).standard_normal((cfg.batch, 1500, cfg.d_model)).astype(np.float32)
+    ckv = wh.CrossKV(cfg.d_model, layers)
+    kv_d = ckv.wh_prepare_cross(torch.from_numpy(mem).cuda())
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    rows = np.sort(np.random.default_rng(12).choice(cfg.batch * 1500, 96, replace=False))
+    rows[-1] = cfg.batch * 1500 - 1
+    pick = [0, 17, 31]
+    kv = kv_d[pick][:, torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    full = np.zeros((len(pick), cfg.batch * 1500, 2 * cfg.d_model), np.float32)
+    full[:, rows] = kv
+    _check_cross(full, mem.reshape(-1, cfg.d_model), [layers[i] for i in pick], rows, "large-v3")
+
+
+@pytest.mark.parametrize("cfg_idx", [0, 1])
+def test_encode_ctx_full_context_is_wh_encode(cfg_idx):
+    cfg = configs.CONFIGS[cfg_idx]
+    enc = wh.Encoder(cfg, synth.weights(cfg))
+    mel = wh.wh_frontend(torch.from_numpy(synth.waveforms(cfg)).cuda(), cfg.n_mels)
+    a = enc.wh_encode(mel)
+    b = enc.wh_encode_ctx(mel, 1500)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("cfg_idx,n_ctx,windows", [(1, 500, [0, 5]), (1, 37, [0]), (2, 501, [3]),
+                                                   (4, 500, [0])])
+def test_encode_ctx_parity(cfg_idx, n_ctx, windows):
+    cfg = configs.CONFIGS[cfg_idx]
+    w = synth.weights(cfg)
+    enc = wh.Encoder(cfg, w)
+    pcm = synth.waveforms(cfg)
+    mel_d = wh.wh_frontend(torch.from_numpy(pcm).cuda(), cfg.n_mels)
+    out = enc.wh_encode_ctx(mel_d, n_ctx)
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    out = out.cpu().numpy()
+    mel = mel_d.cpu().numpy()
+    assert out.shape == (cfg.batch, n_ctx, cfg.d_model) and np.isfinite(out).all()
+    for win in windows:
+        ref = R.encoder_ctx(mel[win], w, cfg.n_head, n_ctx)
+        check_encoder(out[win], ref, f"{cfg.name} n_ctx {n_ctx} window {win}")
+
+
+def test_encode_ctx_ignores_frames_past_its_span():
+    cfg = configs.CONFIGS[1]
+    enc = wh.Encoder(cfg, synth.weights(cfg))
+    mel = wh.wh_frontend(torch.from_numpy(synth.waveforms(cfg)).cuda(), cfg.n_mels)
+    a = enc.wh_encode_ctx(mel, 400).clone()
+    mel[:, 800:] = torch.randn_like(mel[:, 800:])
+    b = enc.wh_encode_ctx(mel, 400)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)

@@ -1,0 +1,99 @@
+"""Pins of the oracle's next rows against facts fixed outside the oracle itself.
+
+Cross-attention keys/values ("whisper 0.9.0 API", model.nu, wh_prepare_cross):
+- A permutation matrix moves columns (a transposed weight would move them the other way).
+- A zero memory gives K = 0 and V = bv (the bias belongs to V, not to K).
+- A zero V projection gives V = bv in every row.
+- A projection built from a known rank-1 pair gives K = (mem a) b^T.
+
+Shorter encoder context (the "whisper" package page, "Serving": whisper.cpp's audio_ctx):
+- n_ctx = 1500 is the full encoder.
+- Frames past 2 n_ctx are never read.
+- The span's end is zero-padded like the end of a window. So the stem equals the full stem
+  of a log-mel whose frames past 2 n_ctx are zero, and rows before the last agree with the
+  full-window stem.
+"""
+import numpy as np
+import pytest
+
+from oracle import whisper_ref as R
+from whisper_audio_encoder_gb300 import synth
+from whisper_audio_encoder_gb300.configs import CONFIGS
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+@pytest.fixture(scope="module")
+def mem():
+    rng = np.random.default_rng(3)
+    return rng.standard_normal((50, 16))
+
+
+def test_cross_kv_moves_columns_by_the_permutation(mem):
+    d = mem.shape[1]
+    perm = np.roll(np.arange(d), 3)                  # not an involution: W and W^T differ
+    w = np.zeros((d, d))
+    w[np.arange(d), perm] = 1.0                      # out column o reads input column perm[o]
+    k, v = R.cross_kv(mem, w, w)
+    np.testing.assert_array_equal(k, mem[:, perm])
+    np.testing.assert_array_equal(v, mem[:, perm])
+    assert not np.allclose(k, mem @ w)               # the transposed operand gives another answer
+
+
+def test_cross_kv_bias_is_on_v_only(mem):
+    d = mem.shape[1]
+    rng = np.random.default_rng(4)
+    wk, wv, bv = rng.standard_normal((d, d)), rng.standard_normal((d, d)), rng.standard_normal(d)
+    k, v = R.cross_kv(np.zeros_like(mem), wk, wv, bv)
+    assert np.all(k == 0.0)
+    np.testing.assert_array_equal(v, np.broadcast_to(bv, v.shape))
+    k2, v2 = R.cross_kv(mem, wk, np.zeros((d, d)), bv)
+    np.testing.assert_array_equal(v2, np.broadcast_to(bv, v2.shape))
+    k3, _ = R.cross_kv(mem, wk, wv, None)
+    np.testing.assert_array_equal(k2, k3)
+
+
+def test_cross_kv_rank_one_projection(mem):
+    d = mem.shape[1]
+    rng = np.random.default_rng(5)
+    a, b = rng.standard_normal(d), rng.standard_normal(d)
+    w = np.outer(b, a)                               # y[o] = b[o] * (a . x)
+    k, _ = R.cross_kv(mem, w, w)
+    np.testing.assert_allclose(k, np.outer(mem @ a, b), rtol=1e-12, atol=1e-12)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    cfg = CONFIGS[0]
+    w = synth.weights(cfg)
+    pcm = synth.waveform(cfg, 0)
+    mel = R.log_mel(pcm, cfg.n_mels)
+    return cfg, w, mel
+
+
+def test_encoder_ctx_full_context_is_the_encoder(tiny):
+    cfg, w, mel = tiny
+    np.testing.assert_array_equal(R.encoder_ctx(mel, w, cfg.n_head, 1500), R.encoder(mel, w, cfg.n_head))
+
+
+@pytest.mark.parametrize("n_ctx", [500, 37])
+def test_encoder_ctx_reads_only_its_span(tiny, n_ctx):
+    cfg, w, mel = tiny
+    out = R.encoder_ctx(mel, w, cfg.n_head, n_ctx)
+    assert out.shape == (n_ctx, cfg.d_model)
+    other = mel.copy()
+    other[2 * n_ctx:] = np.random.default_rng(9).standard_normal(other[2 * n_ctx:].shape)
+    np.testing.assert_array_equal(R.encoder_ctx(other, w, cfg.n_head, n_ctx), out)
+
+
+@pytest.mark.parametrize("n_ctx", [500, 37])
+def test_encoder_ctx_zero_pads_the_end_of_its_span(tiny, n_ctx):
+    cfg, w, mel = tiny
+    short = R.encoder_stem(mel[: 2 * n_ctx], w)
+    zeroed = mel.copy()
+    zeroed[2 * n_ctx:] = 0.0
+    full_zeroed = R.encoder_stem(zeroed, w)[:n_ctx]
+    np.testing.assert_allclose(short, full_zeroed, rtol=1e-12, atol=1e-12)
+    full = R.encoder_stem(mel, w)[:n_ctx]
+    np.testing.assert_allclose(short[:-1], full[:-1], rtol=1e-12, atol=1e-12)  # receptive field inside the span
+    assert np.max(np.abs(short[-1] - full[-1])) > 1e-6     # the last position sees the padding

@@ -1,8 +1,9 @@
 // Non-causal multi-head self-attention, head_dim 64, on the 5th-generation tensor cores
-// ("whisper 0.9.0 API", kernels.nu: attn_f "fused attention, online softmax (hd = 64)",
-// attn_sc "scores = q.k / sqrt(hd), NO causal mask", attn_out "softmax(scores) . v";
-// "How Audio Becomes Words", section "The Encoder: Understand Once": the full 1500 x 1500
-// square, no mask, no RoPE).
+// ("whisper 0.9.0 API", kernels.nu: attn_sc scores each query against every key with the
+// 1/sqrt(64) scale and no causal mask in the encoder, attn_out weights v by the softmax of
+// those scores, attn_f fuses both with an online softmax at head_dim 64;
+// "How Audio Becomes Words", section "The Encoder: Understand Once": every frame attends to
+// the whole 1500 x 1500 square, no mask, no RoPE).
 //
 // Work item = two 128-query tiles (t = 0, 1) of one (window, head); keys stream through in
 // tiles of 128.  One persistent CTA per SM walks the items (window-major, so CTAs running at

@@ -50,7 +50,10 @@ int layernorm_launch(const float *x, int rows, int d, const float *g, const floa
 int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
                      int num_sms, cudaStream_t s);
 int attention_prepare();
-int stem_im2col_launch(const float *mel, int batch, int n_mels, void *a1, cudaStream_t s);
+// conv1's im2col matrix over the first n_frames (<= 3000) frames of each window's log-mel
+int stem_im2col_launch(const float *mel, int batch, int n_mels, int n_frames, void *a1, cudaStream_t s);
+// y (bf16) = x (float32), n a multiple of 4, both 16-byte aligned
+int cast_bf16_launch(const float *x, long long n, void *y, cudaStream_t s);
 int pack_conv_weight_launch(const void *w, int c_out, int c_in, void *wp, cudaStream_t s);
 int selftest_timeout_launch(const DevCtl &ctl, cudaStream_t s);
 
@@ -61,7 +64,7 @@ int device_setup();
 // Kernel classes for the per-kernel timing.
 enum TraceClass {
     TR_FRONTEND = 0, TR_STEM_PREP, TR_GEMM, TR_ATTN, TR_LAYERNORM,
-    TR_GEMM_CONV, TR_GEMM_QKV, TR_GEMM_OUT, TR_GEMM_FC1, TR_GEMM_FC2, TR_NCLASS
+    TR_GEMM_CONV, TR_GEMM_QKV, TR_GEMM_OUT, TR_GEMM_FC1, TR_GEMM_FC2, TR_CROSS_PREP, TR_GEMM_CROSS, TR_NCLASS
 };
 void trace_begin(int cls, cudaStream_t s);
 void trace_end(int cls, cudaStream_t s, double flops, double bytes);

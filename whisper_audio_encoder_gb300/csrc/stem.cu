@@ -15,24 +15,36 @@ namespace {
 
 constexpr int N_FRAMES = 3000;
 
-// a1[b * 3000 + t][j * M + i] = mel[b][t + j - 1][i] (0 outside 0..2999), 8 columns per thread.
+// a1[b * F + t][j * M + i] = mel[b][t + j - 1][i] for the first F = n_frames frames of each
+// window (0 outside 0..F-1: the encoder's zero padding at both ends of the span it reads;
+// windows stay 3000 frames apart in mel), 8 columns per thread.
 __global__ void __launch_bounds__(256) k_mel_im2col(const float *__restrict__ mel, int batch, int n_mels,
-                                                    uint4 *__restrict__ a1) {
+                                                    int n_frames, uint4 *__restrict__ a1) {
     const int groups_per_row = 3 * n_mels / 8;
-    const long long total = (long long)batch * N_FRAMES * groups_per_row;
+    const long long total = (long long)batch * n_frames * groups_per_row;
     for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < total;
          it += (long long)gridDim.x * blockDim.x) {
         const long long row = it / groups_per_row;
         const int gcol = (int)(it - row * groups_per_row) * 8;
         const int j = gcol / n_mels, i = gcol - j * n_mels;
-        const int b = (int)(row / N_FRAMES), t = (int)(row - (long long)b * N_FRAMES) + j - 1;
+        const int b = (int)(row / n_frames), t = (int)(row - (long long)b * n_frames) + j - 1;
         uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (t >= 0 && t < N_FRAMES) {
+        if (t >= 0 && t < n_frames) {
             const float4 *src = reinterpret_cast<const float4 *>(mel + ((long long)b * N_FRAMES + t) * n_mels + i);
             const float4 p = __ldg(src), q = __ldg(src + 1);
             o = make_uint4(pack_bf16(p.x, p.y), pack_bf16(p.z, p.w), pack_bf16(q.x, q.y), pack_bf16(q.z, q.w));
         }
         a1[it] = o;
+    }
+}
+
+// y = bf16(x), 4 values per thread: the encoder memory as the cross-attention GEMMs' operand.
+__global__ void __launch_bounds__(256) k_cast_bf16(const float4 *__restrict__ x, long long n4,
+                                                   uint2 *__restrict__ y) {
+    for (long long it = blockIdx.x * (long long)blockDim.x + threadIdx.x; it < n4;
+         it += (long long)gridDim.x * blockDim.x) {
+        const float4 v = __ldg(x + it);
+        y[it] = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
     }
 }
 
@@ -69,9 +81,19 @@ int grid_for(long long items) {
 
 }  // namespace
 
-int stem_im2col_launch(const float *mel, int batch, int n_mels, void *a1, cudaStream_t s) {
-    const long long items = (long long)batch * N_FRAMES * (3 * n_mels / 8);
-    k_mel_im2col<<<grid_for(items), 256, 0, s>>>(mel, batch, n_mels, reinterpret_cast<uint4 *>(a1));
+int stem_im2col_launch(const float *mel, int batch, int n_mels, int n_frames, void *a1, cudaStream_t s) {
+    if (n_frames <= 0 || n_frames > N_FRAMES) return WH_EINVAL;
+    const long long items = (long long)batch * n_frames * (3 * n_mels / 8);
+    k_mel_im2col<<<grid_for(items), 256, 0, s>>>(mel, batch, n_mels, n_frames, reinterpret_cast<uint4 *>(a1));
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
+}
+
+int cast_bf16_launch(const float *x, long long n, void *y, cudaStream_t s) {
+    if (n <= 0) return WH_OK;
+    if (n % 4 != 0) return WH_EINVAL;
+    k_cast_bf16<<<grid_for(n / 4), 256, 0, s>>>(reinterpret_cast<const float4 *>(x), n / 4,
+                                                 reinterpret_cast<uint2 *>(y));
     count_launch();
     return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
 }

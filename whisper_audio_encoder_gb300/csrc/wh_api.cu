@@ -81,8 +81,9 @@ struct TraceRec {
     cudaEvent_t e0, e1;
     double flops, bytes;
 };
-const char *const kTraceNames[TR_NCLASS] = {"frontend", "stem_prep", "gemm", "attention", "layernorm",
-                                             "gemm_conv", "gemm_qkv", "gemm_out", "gemm_fc1", "gemm_fc2"};
+const char *const kTraceNames[TR_NCLASS] = {"frontend", "stem_prep", "gemm",       "attention",
+                                             "layernorm", "gemm_conv", "gemm_qkv",   "gemm_out",
+                                             "gemm_fc1",  "gemm_fc2",  "cross_prep", "gemm_cross"};
 std::mutex g_tr_mu;
 bool g_tr_on = false;
 std::vector<TraceRec> g_tr;
@@ -115,8 +116,9 @@ struct EncLayout {
     size_t x, xn, qkv, ao, h, a1, w1p, w2p, total;
 };
 
-EncLayout layout(const wh_config *c, int batch) {
-    const size_t rows = (size_t)batch * N_CTX, d = c->d_model, f = c->d_ff, M = c->n_mels;
+// n_ctx encoder positions per window (conv1 runs over 2 n_ctx log-mel frames)
+EncLayout layout(const wh_config *c, int batch, int n_ctx) {
+    const size_t rows = (size_t)batch * n_ctx, d = c->d_model, f = c->d_ff, M = c->n_mels;
     EncLayout L;
     size_t off = 0;
     L.x = off;   off += up256(rows * d * 4);
@@ -124,7 +126,7 @@ EncLayout layout(const wh_config *c, int batch) {
     L.qkv = off; off += up256(rows * 3 * d * 2);   // also conv2's im2col matrix
     L.ao = off;  off += up256(rows * d * 2);
     L.h = off;   off += up256(rows * f * 2);
-    L.a1 = off;  off += up256((size_t)batch * N_FRAMES * 3 * M * 2);
+    L.a1 = off;  off += up256((size_t)batch * 2 * n_ctx * 3 * M * 2);
     L.w1p = off; off += up256(d * 3 * M * 2);
     L.w2p = off; off += up256(d * 3 * d * 2);
     L.total = off;
@@ -246,46 +248,51 @@ int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel, 
 
 size_t wh_encode_workspace(const wh_config *cfg, int batch) {
     if (check_config(cfg) != WH_OK || batch <= 0) return 0;
-    return layout(cfg, batch).total;
+    return layout(cfg, batch, N_CTX).total;
 }
 
-int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weights *w, float *out, void *workspace,
-              size_t ws_bytes, void *stream) {
-    if (batch < 0) return WH_EINVAL;
+size_t wh_encode_ctx_workspace(const wh_config *cfg, int batch, int n_ctx) {
+    if (check_config(cfg) != WH_OK || batch <= 0 || n_ctx < 1 || n_ctx > N_CTX) return 0;
+    return layout(cfg, batch, n_ctx).total;
+}
+
+int wh_encode_ctx(const float *mel, int batch, int n_ctx, const wh_config *cfg, const wh_weights *w, float *out,
+                  void *workspace, size_t ws_bytes, void *stream) {
+    if (batch < 0 || n_ctx < 1 || n_ctx > N_CTX) return WH_EINVAL;
     if (int rc = check_config(cfg)) return rc;
     if (batch == 0) return WH_OK;
     if (!mel || !out || !workspace || !aligned(mel, 16) || !aligned(out, 16) || !aligned(workspace, 256))
         return WH_EINVAL;
     if (int rc = check_weights(cfg, w)) return rc;
-    const EncLayout L = layout(cfg, batch);
+    const EncLayout L = layout(cfg, batch, n_ctx);
     if (ws_bytes < L.total) return WH_ENOSPC;
     DevState *st;
     if (int rc = ensure_device(&st)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     const int d = cfg->d_model, f = cfg->d_ff, M = cfg->n_mels, H = cfg->n_head;
-    const int rows = batch * N_CTX;
+    const int rows = batch * n_ctx, n_frames = 2 * n_ctx;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *x = reinterpret_cast<float *>(ws + L.x);
     void *xn = ws + L.xn, *qkv = ws + L.qkv, *ao = ws + L.ao, *hb = ws + L.h, *a1 = ws + L.a1;
     void *w1p = ws + L.w1p, *w2p = ws + L.w2p;
     int rc;
 
-    // ---- conv stem
+    // ---- conv stem over the first 2 n_ctx frames of each window
     trace_begin(TR_STEM_PREP, s);
     if ((rc = pack_conv_weight_launch(w->conv1_w, d, M, w1p, s))) return rc;
     if ((rc = pack_conv_weight_launch(w->conv2_w, d, d, w2p, s))) return rc;
-    if ((rc = stem_im2col_launch(mel, batch, M, a1, s))) return rc;
-    trace_end(TR_STEM_PREP, s, 0.0, (double)batch * N_FRAMES * M * (4.0 + 6.0));
+    if ((rc = stem_im2col_launch(mel, batch, M, n_frames, a1, s))) return rc;
+    trace_end(TR_STEM_PREP, s, 0.0, (double)batch * n_frames * M * (4.0 + 6.0));
     {
-        GemmDesc g = gemm(a1, 3 * M, batch * N_FRAMES, 3 * M, w1p, 3 * M, d, w->conv1_b, qkv, 3LL * d);
-        g.rows_per_win = N_FRAMES;
+        GemmDesc g = gemm(a1, 3 * M, batch * n_frames, 3 * M, w1p, 3 * M, d, w->conv1_b, qkv, 3LL * d);
+        g.rows_per_win = n_frames;
         if ((rc = run_gemm(g, GEMM_CONV1, st, s, TR_GEMM_CONV))) return rc;
     }
     {
         GemmDesc g = gemm(qkv, 3 * d, rows, 3 * d, w2p, 3 * d, d, w->conv2_b, x, d);
-        g.pos = w->pos;
-        g.rows_per_win = N_CTX;
+        g.pos = w->pos;  // its first n_ctx rows
+        g.rows_per_win = n_ctx;
         if ((rc = run_gemm(g, GEMM_CONV2, st, s, TR_GEMM_CONV))) return rc;
     }
     // ---- blocks
@@ -304,8 +311,8 @@ int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weight
             if ((rc = run_gemm(g, GEMM_BF16, st, s, TR_GEMM_QKV))) return rc;
         }
         trace_begin(TR_ATTN, s);
-        if ((rc = attention_launch(qkv, batch, N_CTX, H, ao, ctl_of(st), st->num_sms, s))) return rc;
-        trace_end(TR_ATTN, s, 4.0 * batch * (double)N_CTX * N_CTX * d, (double)rows * d * 8.0);
+        if ((rc = attention_launch(qkv, batch, n_ctx, H, ao, ctl_of(st), st->num_sms, s))) return rc;
+        trace_end(TR_ATTN, s, 4.0 * batch * (double)n_ctx * n_ctx * d, (double)rows * d * 8.0);
         if ((rc = run_gemm(gemm(ao, d, rows, d, Lw.wo, d, d, Lw.bo, x, d), GEMM_RESID_F32, st, s, TR_GEMM_OUT)))
             return rc;
         trace_begin(TR_LAYERNORM, s);
@@ -320,6 +327,46 @@ int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weight
     rc = layernorm_launch(x, rows, d, w->lnf_g, w->lnf_b, out, 0, s);
     trace_end(TR_LAYERNORM, s, 0.0, (double)rows * d * 8.0);
     return rc;
+}
+
+int wh_encode(const float *mel, int batch, const wh_config *cfg, const wh_weights *w, float *out, void *workspace,
+              size_t ws_bytes, void *stream) {
+    return wh_encode_ctx(mel, batch, N_CTX, cfg, w, out, workspace, ws_bytes, stream);
+}
+
+size_t wh_prepare_cross_workspace(int batch, int n_ctx, int d_model) {
+    if (batch <= 0 || n_ctx < 1 || n_ctx > N_CTX || d_model < 128 || d_model > 2048 || d_model % 128 != 0) return 0;
+    return up256((size_t)batch * n_ctx * d_model * 2);
+}
+
+int wh_prepare_cross(const float *mem, int batch, int n_ctx, int d_model, int n_layer, const wh_cross_weights *w,
+                     wh_bf16 *kv, void *workspace, size_t ws_bytes, void *stream) {
+    if (batch < 0 || n_ctx < 1 || n_ctx > N_CTX || n_layer < 0) return WH_EINVAL;
+    if (d_model < 128 || d_model > 2048 || d_model % 128 != 0) return WH_EINVAL;
+    if (batch == 0 || n_layer == 0) return WH_OK;
+    if (!mem || !kv || !workspace || !w || !w->wk || !w->wv || !w->bv) return WH_EINVAL;
+    if (!aligned(mem, 16) || !aligned(kv, 16) || !aligned(workspace, 256)) return WH_EINVAL;
+    for (int l = 0; l < n_layer; ++l)
+        if (!mat_ok(w->wk[l]) || !mat_ok(w->wv[l]) || (w->bv[l] != nullptr && !aligned(w->bv[l], 16)))
+            return WH_EINVAL;
+    if (ws_bytes < wh_prepare_cross_workspace(batch, n_ctx, d_model)) return WH_ENOSPC;
+    DevState *st;
+    if (int rc = ensure_device(&st)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int d = d_model, rows = batch * n_ctx;
+    trace_begin(TR_CROSS_PREP, s);
+    int rc = cast_bf16_launch(mem, (long long)rows * d, workspace, s);
+    trace_end(TR_CROSS_PREP, s, 0.0, (double)rows * d * 6.0);
+    if (rc) return rc;
+    for (int l = 0; l < n_layer; ++l) {
+        // one GEMM per decoder layer, two output segments: [K | V] = mem [Wk; Wv]^T + [0; bv]
+        GemmDesc g = gemm(workspace, d, rows, d, w->wk[l], d, 2 * d, nullptr, kv + (size_t)l * rows * 2 * d, 2LL * d);
+        g.b[1] = w->wv[l];
+        g.seg_n = d;
+        g.bias[1] = w->bv[l];
+        if ((rc = run_gemm(g, GEMM_BF16, st, s, TR_GEMM_CROSS))) return rc;
+    }
+    return WH_OK;
 }
 
 int wh_layer_norm(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,

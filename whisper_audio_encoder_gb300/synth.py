@@ -153,6 +153,20 @@ def weights(cfg: EncoderConfig, layers=None) -> dict:
     return w
 
 
+def cross_weights(cfg: EncoderConfig, n_layer=None) -> list:
+    """Cross-attention k/v projections of the decoder layers (Whisper's decoder has as many
+    layers as its encoder): wk, wv N(0, 0.02) rounded to bf16, bv N(0, 0.01).  Layer l's
+    tensors use the seed sequence (7 + c, 1000 + l, t)."""
+    n = cfg.n_layer if n_layer is None else n_layer
+    d = cfg.d_model
+    out = []
+    for l in range(n):
+        out.append({"wk": bf16_round(_normal(_rng(cfg, 1000 + l, 0), (d, d), 0.02)),
+                    "wv": bf16_round(_normal(_rng(cfg, 1000 + l, 1), (d, d), 0.02)),
+                    "bv": _normal(_rng(cfg, 1000 + l, 2), (d,), 0.01).astype(np.float32)})
+    return out
+
+
 def random_weights(n_mels, d_model, n_layer, d_ff, seed, ln_random=False) -> dict:
     """Weights of an arbitrary (test-sized) encoder, same distributions as the workloads.
     With ln_random the LayerNorm gamma/beta are drawn too (so a swapped or dropped

@@ -35,6 +35,10 @@ class wh_weights(ctypes.Structure):
                 ("layers", ctypes.POINTER(wh_layer_weights)), ("lnf_g", _p), ("lnf_b", _p)]
 
 
+class wh_cross_weights(ctypes.Structure):
+    _fields_ = [("wk", ctypes.POINTER(_p)), ("wv", ctypes.POINTER(_p)), ("bv", ctypes.POINTER(_p))]
+
+
 class wh_trace_stat(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double),
                 ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
@@ -65,6 +69,12 @@ def lib():
         "wh_encode_workspace": (ctypes.c_size_t, [ctypes.POINTER(wh_config), ctypes.c_int]),
         "wh_encode": (ctypes.c_int, [_p, ctypes.c_int, ctypes.POINTER(wh_config), ctypes.POINTER(wh_weights),
                                      _p, _p, ctypes.c_size_t, _p]),
+        "wh_encode_ctx_workspace": (ctypes.c_size_t, [ctypes.POINTER(wh_config), ctypes.c_int, ctypes.c_int]),
+        "wh_encode_ctx": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, ctypes.POINTER(wh_config),
+                                         ctypes.POINTER(wh_weights), _p, _p, ctypes.c_size_t, _p]),
+        "wh_prepare_cross_workspace": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+        "wh_prepare_cross": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.POINTER(wh_cross_weights), _p, _p, ctypes.c_size_t, _p]),
         "wh_layer_norm": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, _p, _p, _p, ctypes.c_int, _p]),
         "wh_linear": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, _p, ctypes.c_int, _p, ctypes.c_int, _p, _p]),
         "wh_attention": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _p, _p]),
@@ -228,12 +238,12 @@ class Encoder:
         self._ws = None
         self._fe_ws = None
 
-    def workspace_bytes(self, batch: int) -> int:
-        return lib().wh_encode_workspace(ctypes.byref(self.c_cfg), batch)
+    def workspace_bytes(self, batch: int, n_ctx: int = N_CTX) -> int:
+        return lib().wh_encode_ctx_workspace(ctypes.byref(self.c_cfg), batch, n_ctx)
 
-    def workspace(self, batch: int):
+    def workspace(self, batch: int, n_ctx: int = N_CTX):
         import torch
-        need = self.workspace_bytes(batch)
+        need = self.workspace_bytes(batch, n_ctx)
         if self._ws is None or self._ws.numel() < need:
             self._ws = None
             self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
@@ -249,6 +259,19 @@ class Encoder:
         rc = lib().wh_encode(_ptr(mel), batch, ctypes.byref(self.c_cfg), ctypes.byref(self.c_w), _ptr(out),
                              _ptr(ws), ws.numel(), _stream(stream))
         _check(rc, "wh_encode")
+        return out
+
+    def wh_encode_ctx(self, mel, n_ctx: int, out=None, stream=None):
+        """The encoder over the first 2 n_ctx frames of each window's log-mel:
+        mel float32 [batch][3000][n_mels] (device) -> float32 [batch][n_ctx][d_model]."""
+        import torch
+        batch = mel.shape[0]
+        if out is None:
+            out = torch.empty(batch, n_ctx, self.cfg.d_model, dtype=torch.float32, device=self.device)
+        ws = self.workspace(batch, n_ctx)
+        rc = lib().wh_encode_ctx(_ptr(mel), batch, n_ctx, ctypes.byref(self.c_cfg), ctypes.byref(self.c_w),
+                                 _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+        _check(rc, "wh_encode_ctx")
         return out
 
     def frontend_workspace(self, batch: int):
@@ -307,3 +330,50 @@ class Graph:
             self.destroy()
         except Exception:
             pass
+
+
+# ---------------------------------------------------------------------------------------
+# Cross-attention K/V of the decoder layers (wh_prepare_cross)
+# ---------------------------------------------------------------------------------------
+class CrossKV:
+    """Holds the decoder layers' cross-attention k/v projections on the device and calls
+    wh_prepare_cross.  `layers` is a list of dicts with "wk", "wv" (bf16-representable
+    float32 [d][d]) and "bv" (float32 [d] or None)."""
+
+    def __init__(self, d_model: int, layers, device="cuda"):
+        import torch
+        self.d_model = d_model
+        self.n_layer = len(layers)
+        self.device = torch.device(device)
+        self._keep = []
+
+        def put(a, dtype):
+            t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dtype).to(self.device)
+            self._keep.append(t)
+            return t.data_ptr()
+
+        n = max(1, self.n_layer)
+        self._wk, self._wv, self._bv = (_p * n)(), (_p * n)(), (_p * n)()
+        for i, lw in enumerate(layers):
+            self._wk[i] = put(lw["wk"], torch.bfloat16)
+            self._wv[i] = put(lw["wv"], torch.bfloat16)
+            self._bv[i] = None if lw.get("bv") is None else put(lw["bv"], torch.float32)
+        self.c_w = wh_cross_weights(ctypes.cast(self._wk, ctypes.POINTER(_p)), ctypes.cast(self._wv, ctypes.POINTER(_p)),
+                                    ctypes.cast(self._bv, ctypes.POINTER(_p)))
+        self._ws = None
+
+    def wh_prepare_cross(self, mem, kv=None, stream=None):
+        """mem float32 [batch][n_ctx][d] (device) -> kv bf16 [n_layer][batch * n_ctx][2 d]:
+        K in columns 0..d-1, V in d..2d-1."""
+        import torch
+        batch, n_ctx, d = mem.shape
+        assert d == self.d_model and mem.dtype == torch.float32 and mem.is_contiguous()
+        if kv is None:
+            kv = torch.empty(self.n_layer, batch * n_ctx, 2 * d, dtype=torch.bfloat16, device=self.device)
+        need = max(256, lib().wh_prepare_cross_workspace(batch, n_ctx, d))
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        rc = lib().wh_prepare_cross(_ptr(mem), batch, n_ctx, d, self.n_layer, ctypes.byref(self.c_w), _ptr(kv),
+                                    _ptr(self._ws), self._ws.numel(), _stream(stream))
+        _check(rc, "wh_prepare_cross")
+        return kv
