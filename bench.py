@@ -261,6 +261,30 @@ def _time_next(enc, cfg, B, pcm_d, mel_d, out_d, steps):
                        "tflops": flops / (ms * 1e-3) / 1e12, "decoder_layers": ckv.n_layer,
                        "what": "wh_prepare_cross: K, V of every decoder layer from the batch's encoder memory"}
     del kv, ckv
+    # one decoder step's cross-attention of one layer: one query per (window, head) over the
+    # 1500 keys and values of that layer's [K | V] rows.  Calls cycle over 4 layers (4 x 123 MB
+    # for large-v3), so each call's K/V comes from HBM, not from the 129 MB L2.
+    kv4 = wh.CrossKV(d, synth.cross_weights(cfg, 4)).wh_prepare_cross(out_d)
+    qd = torch.randn(B, d, device="cuda").to(torch.bfloat16)
+    ws_da = torch.empty(max(256, wh.lib().wh_decode_attention_workspace(B, cfg.n_head, 1500)),
+                        dtype=torch.uint8, device="cuda")
+    o_da = torch.empty(B, d, dtype=torch.bfloat16, device="cuda")
+    calls = [0]
+
+    def one_step():
+        kvl = kv4[calls[0] % 4]
+        calls[0] += 1
+        wh.wh_decode_attention(qd, kvl, kvl[:, d:], 2 * d, 1500 * 2 * d, 1500, cfg.n_head, out=o_da,
+                               workspace=ws_da)
+    ms = timed(one_step, 200)
+    nbytes = B * 1500 * 2 * d * 2.0
+    peaks = _peaks()
+    res["decode_attention"] = {"us_per_call": ms * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                               "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                               "keys": 1500, "sequences": B, "heads": cfg.n_head,
+                               "what": "wh_decode_attention: one decoder step's cross-attention of one layer "
+                                       "(K and V read once: 1500 x 2 d bf16 per window)"}
+    del kv4
     n_ctx = 500  # a draft over 5 s of audio + 5 s: the 10-s minimum
     out_ctx = torch.empty(B, n_ctx, d, device="cuda")
     fe_ws = enc.frontend_workspace(B)

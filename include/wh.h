@@ -223,6 +223,30 @@ int wh_linear(const wh_bf16 *a, int rows, int k, const wh_bf16 *w, int n, const 
 int wh_attention(const wh_bf16 *qkv, int batch, int n_ctx, int n_head, wh_bf16 *out,
                  void *stream);
 
+/* One-query attention of a decoder step ("whisper" package page, "Performance and memory":
+ * a decode step has one query per head, so the keys are split across blocks and the blocks'
+ * partial softmaxes are merged; "whisper 0.9.0 API", wh_decode_step: with the single query at
+ * the end, the decoder's self-attention needs no mask, and its cross-attention reads every
+ * encoder position).  For each sequence b and head h:
+ *   out[b][64 h ..] = softmax(q[b][64 h ..] . K_b,h^T / sqrt(64)) V_b,h    over n_keys[b] keys
+ *   q     device bf16 [batch][64 n_head]
+ *   k, v  device bf16: key t of sequence b, head h is the 64 values at
+ *         k + b * seq_stride + t * row_stride + 64 h (likewise v).  wh_prepare_cross's rows
+ *         give row_stride = 2 d_model, seq_stride = n_ctx * 2 d_model, v = k + d_model; a
+ *         self-attention cache [batch][max][d_model] gives row_stride = d_model.
+ *   n_keys  device int32 [batch] (each clamped to 0 .. max_keys), or NULL: max_keys for all.
+ *         A sequence with no keys gets zeros.
+ *   out   device bf16 [batch][64 n_head]
+ *   workspace  >= wh_decode_attention_workspace(batch, n_head, max_keys) bytes, 256-byte
+ *         aligned, contents need not be initialised; not shared by concurrent calls.
+ *   row_stride >= 64 n_head and seq_stride >= 0, both multiples of 8 elements; pointers
+ *   16-byte aligned; 1 <= max_keys <= 2^30; batch, n_head <= 65535.
+ * Errors: WH_EINVAL, WH_ENOSPC, WH_ECUDA.  batch == 0 is a no-op. */
+size_t wh_decode_attention_workspace(int batch, int n_head, int max_keys);
+int wh_decode_attention(const wh_bf16 *q, const wh_bf16 *k, const wh_bf16 *v, int64_t row_stride,
+                        int64_t seq_stride, const int *n_keys, int max_keys, int batch, int n_head,
+                        wh_bf16 *out, void *workspace, size_t ws_bytes, void *stream);
+
 /* ---------------------------------------------------------------------------------------
  * Status, errors, tracing
  * ------------------------------------------------------------------------------------ */

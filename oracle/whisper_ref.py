@@ -260,3 +260,23 @@ def cross_kv(mem: np.ndarray, wk: np.ndarray, wv: np.ndarray, bv=None):
     if bv is not None:
         v = v + _f64(bv)
     return k, v
+
+
+# ========================================================================================
+# One-query attention of a decoder step  [README] "Performance and memory"; [API] wh_decode_step
+# ========================================================================================
+def attend_one(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_head: int) -> np.ndarray:
+    """A single query per head against all the given keys, no mask (the one query sits at the
+    end of the sequence): q [n_head * 64], k / v [n_keys][n_head * 64] -> [n_head * 64].
+    With no keys the result is zeros (the softmax of an empty set is undefined)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    hd = q.shape[0] // n_head
+    out = np.zeros(q.shape[0], dtype=np.float64)
+    if k.shape[0] == 0:
+        return out
+    for h in range(n_head):
+        sl = slice(h * hd, (h + 1) * hd)
+        s = k[:, sl] @ q[sl] / np.sqrt(hd)
+        p = np.exp(s - s.max())
+        out[sl] = (p / p.sum()) @ v[:, sl]
+    return out

@@ -163,3 +163,27 @@ def test_prepare_cross_rejects_bad_arguments(L):
     assert L.wh_prepare_cross(FAKE, 2, 1500, 384, 2, ctypes.byref(cw), FAKE, FAKE, 16, None) == wh.WH_ENOSPC
     assert L.wh_prepare_cross(FAKE, 0, 1500, 384, 2, ctypes.byref(cw), FAKE, FAKE, 0, None) == wh.WH_OK
     assert L.wh_prepare_cross(FAKE, 2, 1500, 384, 0, ctypes.byref(cw), FAKE, FAKE, 0, None) == wh.WH_OK
+
+
+def test_decode_attention_rejects_bad_arguments(L):
+    ws = 1 << 30
+    assert L.wh_decode_attention_workspace(2, 6, 1500) > 2 * 6 * 66 * 4
+    good = (FAKE, FAKE, FAKE, 384, 384 * 1500, None, 1500, 2, 6, FAKE, FAKE, ws, None)
+    bad = [dict(i=3, x=100),            # row stride below 64 n_head
+           dict(i=3, x=388),            # row stride not a multiple of 8
+           dict(i=4, x=-8),             # negative sequence stride
+           dict(i=4, x=12),             # sequence stride not a multiple of 8
+           dict(i=6, x=0),              # no keys at all
+           dict(i=7, x=-1), dict(i=7, x=70000), dict(i=8, x=0),
+           dict(i=0, x=None), dict(i=9, x=None),
+           dict(i=1, x=ctypes.c_void_p((1 << 20) + 4))]
+    for case in bad:
+        args = list(good)
+        args[case["i"]] = case["x"]
+        assert L.wh_decode_attention(*args) == wh.WH_EINVAL, case
+    args = list(good)
+    args[11] = 64
+    assert L.wh_decode_attention(*args) == wh.WH_ENOSPC
+    args = list(good)
+    args[7] = 0
+    assert L.wh_decode_attention(*args) == wh.WH_OK

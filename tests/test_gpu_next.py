@@ -10,6 +10,12 @@ wh_prepare_cross: the cross-attention keys/values of every decoder layer.
 wh_encode_ctx: the encoder over the first 2 n_ctx log-mel frames.
 - n_ctx = 1500 is bitwise wh_encode.
 - Shorter contexts are held to the encoder bar against the oracle's encoder_ctx.
+
+wh_decode_attention: one query per (sequence, head), keys split across blocks and merged.
+- Against the oracle's attend_one: bf16 output rounding, 2^-8 |ref| + 1e-4 max|v|.
+- Layouts: dense caches, wh_prepare_cross's [K | V] rows, and a ragged self-attention cache
+  with an empty sequence.
+- Many splits: 20 000 keys.
 """
 import numpy as np
 import pytest
@@ -131,5 +137,88 @@ def test_encode_ctx_ignores_frames_past_its_span():
     a = enc.wh_encode_ctx(mel, 400).clone()
     mel[:, 800:] = torch.randn_like(mel[:, 800:])
     b = enc.wh_encode_ctx(mel, 400)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ---- one-query attention of a decoder step --------------------------------------------------
+def _check_attend(out, q, k_rows, v_rows, n_head, what):
+    """out bf16 result (numpy float32) of one sequence; q, k_rows, v_rows float32 (bf16 values)."""
+    ref = R.attend_one(q, k_rows, v_rows, n_head)
+    vmax = float(np.max(np.abs(v_rows))) if v_rows.size else 0.0
+    bad = np.abs(out - ref) > 2.0 ** -8 * np.abs(ref) + 1e-4 * max(vmax, 1.0)
+    assert not bad.any(), f"{what}: {bad.sum()} outside, max {np.max(np.abs(out - ref)):.3e}"
+
+
+@pytest.mark.parametrize("batch,n_head,n_keys", [(1, 6, 1500), (3, 8, 37), (2, 20, 1500), (1, 1, 1), (2, 4, 20000)])
+def test_decode_attention_dense_cache(batch, n_head, n_keys):
+    """K and V as separate [batch][n_keys][64 n_head] caches, every sequence full."""
+    rng = np.random.default_rng(batch * 7 + n_head + n_keys)
+    D = 64 * n_head
+    q = bf16_round_np(rng.standard_normal((batch, D)))
+    k = bf16_round_np(rng.standard_normal((batch, n_keys, D)))
+    v = bf16_round_np(rng.standard_normal((batch, n_keys, D)))
+    dev = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
+    out = wh.wh_decode_attention(dev(q), dev(k), dev(v), D, n_keys * D, n_keys, n_head)
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    out = out.float().cpu().numpy()
+    for b in range(batch):
+        _check_attend(out[b], q[b], k[b], v[b], n_head, f"sequence {b}")
+
+
+def test_decode_attention_over_prepare_cross_rows():
+    """The cross-attention of one decoder layer straight off wh_prepare_cross's [K | V] rows."""
+    cfg = configs.CONFIGS[1]
+    d, H = cfg.d_model, cfg.n_head
+    layers = synth.cross_weights(cfg, 2)
+    rng = np.random.default_rng(30)
+    mem = rng.standard_normal((3, 1500, d)).astype(np.float32)
+    kv = wh.CrossKV(d, layers).wh_prepare_cross(torch.from_numpy(mem).cuda())
+    q = bf16_round_np(rng.standard_normal((3, d)))
+    l = 1
+    kl = kv[l]                                        # [3 * 1500][2 d]
+    out = wh.wh_decode_attention(torch.from_numpy(q).to(torch.bfloat16).cuda(), kl, kl[:, d:], 2 * d,
+                                 1500 * 2 * d, 1500, H)
+    torch.cuda.synchronize()
+    out = out.float().cpu().numpy()
+    kvn = kl.float().cpu().numpy()
+    for b in range(3):
+        rows = kvn[b * 1500:(b + 1) * 1500]
+        _check_attend(out[b], q[b], rows[:, :d], rows[:, d:], H, f"cross window {b}")
+
+
+def test_decode_attention_ragged_self_cache():
+    """A self-attention cache [batch][448][d] with a different length per sequence (0 included)."""
+    n_head, cap = 6, 448
+    D = 64 * n_head
+    lens = np.array([1, 448, 0, 130, 447], dtype=np.int32)
+    rng = np.random.default_rng(31)
+    q = bf16_round_np(rng.standard_normal((len(lens), D)))
+    k = bf16_round_np(rng.standard_normal((len(lens), cap, D)))
+    v = bf16_round_np(rng.standard_normal((len(lens), cap, D)))
+    dev = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
+    out = wh.wh_decode_attention(dev(q), dev(k), dev(v), D, cap * D, cap, n_head,
+                                 n_keys=torch.from_numpy(lens).cuda())
+    torch.cuda.synchronize()
+    out = out.float().cpu().numpy()
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert np.all(out[b] == 0.0)
+        else:
+            _check_attend(out[b], q[b], k[b, :n], v[b, :n], n_head, f"sequence {b} ({n} keys)")
+
+
+def test_decode_attention_repeated_calls_reuse_the_workspace():
+    """The merge tickets are reset by each call: the same workspace gives the same result."""
+    rng = np.random.default_rng(32)
+    D, n = 64 * 20, 1500
+    q = torch.from_numpy(bf16_round_np(rng.standard_normal((16, D)))).to(torch.bfloat16).cuda()
+    k = torch.from_numpy(bf16_round_np(rng.standard_normal((16, n, D)))).to(torch.bfloat16).cuda()
+    v = torch.from_numpy(bf16_round_np(rng.standard_normal((16, n, D)))).to(torch.bfloat16).cuda()
+    ws = torch.empty(wh.lib().wh_decode_attention_workspace(16, 20, n), dtype=torch.uint8, device="cuda")
+    a = wh.wh_decode_attention(q, k, v, D, n * D, n, 20, workspace=ws).clone()
+    for _ in range(3):
+        b = wh.wh_decode_attention(q, k, v, D, n * D, n, 20, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(a, b)

@@ -97,3 +97,47 @@ def test_encoder_ctx_zero_pads_the_end_of_its_span(tiny, n_ctx):
     full = R.encoder_stem(mel, w)[:n_ctx]
     np.testing.assert_allclose(short[:-1], full[:-1], rtol=1e-12, atol=1e-12)  # receptive field inside the span
     assert np.max(np.abs(short[-1] - full[-1])) > 1e-6     # the last position sees the padding
+
+
+# ---- one-query attention of a decoder step ------------------------------------------------
+def test_attend_one_equal_keys_give_the_mean_of_v():
+    rng = np.random.default_rng(20)
+    n_head, n = 3, 17
+    q = rng.standard_normal(64 * n_head)
+    k = np.tile(rng.standard_normal(64 * n_head), (n, 1))
+    v = rng.standard_normal((n, 64 * n_head))
+    np.testing.assert_allclose(R.attend_one(q, k, v, n_head), v.mean(axis=0), rtol=1e-12, atol=1e-12)
+
+
+def test_attend_one_dominant_key_selects_its_value():
+    rng = np.random.default_rng(21)
+    n_head, n, j = 2, 40, 23
+    k = rng.standard_normal((n, 64 * n_head)) * 0.01
+    q = np.zeros(64 * n_head)
+    q[0], q[64] = 1.0, 1.0
+    k[j, 0], k[j, 64] = 800.0, 800.0        # score 100 above the rest after the 1/8 scale
+    v = rng.standard_normal((n, 64 * n_head))
+    np.testing.assert_allclose(R.attend_one(q, k, v, n_head), v[j], rtol=1e-12, atol=1e-12)
+
+
+def test_attend_one_ignores_key_order_single_key_and_empty():
+    rng = np.random.default_rng(22)
+    n_head, n = 4, 33
+    q, k, v = rng.standard_normal(256), rng.standard_normal((n, 256)), rng.standard_normal((n, 256))
+    perm = rng.permutation(n)
+    np.testing.assert_allclose(R.attend_one(q, k[perm], v[perm], n_head), R.attend_one(q, k, v, n_head),
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(R.attend_one(q, k[:1], v[:1], n_head), v[0], rtol=1e-12, atol=1e-12)
+    assert np.all(R.attend_one(q, k[:0], v[:0], n_head) == 0.0)
+
+
+def test_attend_one_matches_torch_sdpa():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(23)
+    n_head, n = 5, 300
+    q, k, v = rng.standard_normal(320), rng.standard_normal((n, 320)), rng.standard_normal((n, 320))
+    qt = torch.from_numpy(q).reshape(1, n_head, 1, 64)
+    kt = torch.from_numpy(k).reshape(n, n_head, 64).permute(1, 0, 2)[None]
+    vt = torch.from_numpy(v).reshape(n, n_head, 64).permute(1, 0, 2)[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt).reshape(-1).numpy()
+    np.testing.assert_allclose(R.attend_one(q, k, v, n_head), ref, rtol=1e-10, atol=1e-12)

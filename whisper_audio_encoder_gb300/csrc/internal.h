@@ -50,6 +50,11 @@ int layernorm_launch(const float *x, int rows, int d, const float *g, const floa
 int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
                      int num_sms, cudaStream_t s);
 int attention_prepare();
+// one-query attention of a decoder step, keys split across blocks (decode_attention.cu)
+size_t decode_attention_workspace(int batch, int n_head, int max_keys);
+int decode_attention_launch(const void *q, const void *k, const void *v, long long row_stride, long long seq_stride,
+                            const int *n_keys, int max_keys, int batch, int n_head, void *out, void *workspace,
+                            int num_sms, cudaStream_t s);
 // conv1's im2col matrix over the first n_frames (<= 3000) frames of each window's log-mel
 int stem_im2col_launch(const float *mel, int batch, int n_mels, int n_frames, void *a1, cudaStream_t s);
 // y (bf16) = x (float32), n a multiple of 4, both 16-byte aligned
@@ -64,7 +69,7 @@ int device_setup();
 // Kernel classes for the per-kernel timing.
 enum TraceClass {
     TR_FRONTEND = 0, TR_STEM_PREP, TR_GEMM, TR_ATTN, TR_LAYERNORM,
-    TR_GEMM_CONV, TR_GEMM_QKV, TR_GEMM_OUT, TR_GEMM_FC1, TR_GEMM_FC2, TR_CROSS_PREP, TR_GEMM_CROSS, TR_NCLASS
+    TR_GEMM_CONV, TR_GEMM_QKV, TR_GEMM_OUT, TR_GEMM_FC1, TR_GEMM_FC2, TR_CROSS_PREP, TR_GEMM_CROSS, TR_DEC_ATTN, TR_NCLASS
 };
 void trace_begin(int cls, cudaStream_t s);
 void trace_end(int cls, cudaStream_t s, double flops, double bytes);

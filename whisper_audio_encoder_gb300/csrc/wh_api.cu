@@ -83,7 +83,8 @@ struct TraceRec {
 };
 const char *const kTraceNames[TR_NCLASS] = {"frontend", "stem_prep", "gemm",       "attention",
                                              "layernorm", "gemm_conv", "gemm_qkv",   "gemm_out",
-                                             "gemm_fc1",  "gemm_fc2",  "cross_prep", "gemm_cross"};
+                                             "gemm_fc1",  "gemm_fc2",  "cross_prep", "gemm_cross",
+                                             "decode_attention"};
 std::mutex g_tr_mu;
 bool g_tr_on = false;
 std::vector<TraceRec> g_tr;
@@ -367,6 +368,34 @@ int wh_prepare_cross(const float *mem, int batch, int n_ctx, int d_model, int n_
         if ((rc = run_gemm(g, GEMM_BF16, st, s, TR_GEMM_CROSS))) return rc;
     }
     return WH_OK;
+}
+
+size_t wh_decode_attention_workspace(int batch, int n_head, int max_keys) {
+    if (batch > 65535 || n_head > 65535 || max_keys > (1 << 30)) return 0;
+    return decode_attention_workspace(batch, n_head, max_keys);
+}
+
+int wh_decode_attention(const wh_bf16 *q, const wh_bf16 *k, const wh_bf16 *v, int64_t row_stride, int64_t seq_stride,
+                        const int *n_keys, int max_keys, int batch, int n_head, wh_bf16 *out, void *workspace,
+                        size_t ws_bytes, void *stream) {
+    if (batch < 0 || batch > 65535 || n_head < 1 || n_head > 65535 || max_keys < 1 || max_keys > (1 << 30))
+        return WH_EINVAL;
+    if (row_stride < 64LL * n_head || row_stride % 8 != 0 || seq_stride < 0 || seq_stride % 8 != 0) return WH_EINVAL;
+    if (batch == 0) return WH_OK;
+    if (!q || !k || !v || !out || !workspace) return WH_EINVAL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(workspace, 256) ||
+        (n_keys && !aligned(n_keys, 4)))
+        return WH_EINVAL;
+    if (ws_bytes < decode_attention_workspace(batch, n_head, max_keys)) return WH_ENOSPC;
+    DevState *st;
+    if (int rc = ensure_device(&st)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    trace_begin(TR_DEC_ATTN, s);
+    const int rc = decode_attention_launch(q, k, v, row_stride, seq_stride, n_keys, max_keys, batch, n_head, out,
+                                           workspace, st->num_sms, s);
+    trace_end(TR_DEC_ATTN, s, 4.0 * batch * (double)max_keys * 64.0 * n_head,
+              (double)batch * n_head * max_keys * 256.0);
+    return rc;
 }
 
 int wh_layer_norm(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,

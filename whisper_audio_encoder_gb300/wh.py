@@ -75,6 +75,9 @@ def lib():
         "wh_prepare_cross_workspace": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
         "wh_prepare_cross": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.POINTER(wh_cross_weights), _p, _p, ctypes.c_size_t, _p]),
+        "wh_decode_attention_workspace": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+        "wh_decode_attention": (ctypes.c_int, [_p, _p, _p, ctypes.c_int64, ctypes.c_int64, _p, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, _p, _p, ctypes.c_size_t, _p]),
         "wh_layer_norm": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, _p, _p, _p, ctypes.c_int, _p]),
         "wh_linear": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, _p, ctypes.c_int, _p, ctypes.c_int, _p, _p]),
         "wh_attention": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _p, _p]),
@@ -166,6 +169,24 @@ def wh_attention(qkv, batch, n_ctx, n_head, out=None, stream=None):
     if out is None:
         out = torch.empty(batch * n_ctx, n_head * 64, dtype=torch.bfloat16, device=qkv.device)
     _check(lib().wh_attention(_ptr(qkv), batch, n_ctx, n_head, _ptr(out), _stream(stream)), "wh_attention")
+    return out
+
+
+def wh_decode_attention(q, k, v, row_stride, seq_stride, max_keys, n_head, n_keys=None, out=None,
+                        workspace=None, stream=None):
+    """One query per (sequence, head) over up to max_keys keys: q bf16 [batch][64 n_head];
+    k / v bf16 device tensors (views are fine) addressed with the given element strides;
+    n_keys: optional int32 device tensor [batch].  Returns bf16 [batch][64 n_head]."""
+    import torch
+    batch = q.shape[0]
+    if out is None:
+        out = torch.empty(batch, 64 * n_head, dtype=torch.bfloat16, device=q.device)
+    need = max(256, lib().wh_decode_attention_workspace(batch, n_head, max_keys))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = lib().wh_decode_attention(_ptr(q), _ptr(k), _ptr(v), row_stride, seq_stride, _ptr(n_keys), max_keys, batch,
+                                   n_head, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "wh_decode_attention")
     return out
 
 
