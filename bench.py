@@ -296,6 +296,16 @@ def _time_next(enc, cfg, B, pcm_d, mel_d, out_d, steps):
     res["audio_ctx"] = {"n_ctx": n_ctx, "value": B * 1000.0 / ms, "unit": "windows/s", "ms_per_step": ms,
                         "tflops": B * _encoder_flops(cfg, n_ctx) / (ms * 1e-3) / 1e12,
                         "what": "wh_frontend + wh_encode_ctx over the first 10 s of each window"}
+    # resampling 30-s clips recorded at 44.1 kHz to the 16 kHz the front end takes
+    x441 = torch.randn(B, 44100 * 30, device="cuda")
+    y16 = torch.empty(B, wh.lib().wh_resample_length(44100 * 30, 44100), device="cuda")
+    ws_rs = torch.empty(max(256, wh.lib().wh_resample_workspace(44100)), dtype=torch.uint8, device="cuda")
+    ms = timed(lambda: wh.wh_resample(x441, 44100, y=y16, workspace=ws_rs), max(5, steps))
+    nbytes = (x441.numel() + y16.numel()) * 4.0
+    res["resample"] = {"value": B * 1000.0 / ms, "unit": "windows/s", "ms_per_batch": ms,
+                       "gbs": nbytes / (ms * 1e-3) / 1e9, "rate_in": 44100,
+                       "what": "wh_resample: B 30-s clips, 44.1 kHz -> 16 kHz (windowed-sinc polyphase)"}
+    del x441, y16
     st = wh.wh_status()
     if st != wh.WH_OK:
         raise RuntimeError(f"device status after the next-row measurements: {wh.wh_strerror(st)}")

@@ -94,6 +94,41 @@ int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel,
                 void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Front end of one long clip ("whisper 0.9.0 API", main.nu, wh_run: audio longer than 30 s is
+ * cut into 30-s windows, each encoded -- and decoded -- on its own).  Window w holds samples
+ * [480000 w, 480000 (w + 1)) of the clip, the last one zero-padded; each window gets its own
+ * log-mel exactly as wh_frontend computes it (own reflect padding, own maximum and clamp).
+ *   wh_frontend_windows(n_total) = ceil(n_total / 480000) (0 for an empty clip).
+ *   pcm   device float32 [n_total], 16-byte aligned
+ *   mel   device float32 [wh_frontend_windows(n_total)][3000][n_mels]
+ *   workspace >= wh_frontend_workspace(windows) bytes, 16-byte aligned.
+ * Errors: WH_EINVAL (null or misaligned pointer, n_total < 0, more than 65535 windows, n_mels
+ * not 80/128), WH_ENOSPC, WH_ECUDA.  An empty clip is a no-op.
+ * ------------------------------------------------------------------------------------ */
+int64_t wh_frontend_windows(int64_t n_total);
+int wh_frontend_long(const float *pcm, int64_t n_total, int n_mels, float *mel, void *workspace,
+                     size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Resampling to 16 kHz ("whisper" package page, "Transcribing": input at any rate is
+ * resampled to 16 kHz with a windowed sinc, not linear interpolation; "How it is verified":
+ * checked against scipy's resample_poly).  The filter is resample_poly's default design: with
+ * up / down = 16000 / rate_in in lowest terms and M = max(up, down), a Kaiser-windowed
+ * (beta 5) sinc low-pass at 1 / M of the upsampled Nyquist rate, 20 M + 1 taps, unit DC gain,
+ * times up; y[j] = sum_i h[j down + 10 M - i up] x[i] (zero phase, x = 0 outside the clip).
+ *   wh_resample_length(n_in, rate_in) = ceil(n_in * up / down) output samples (-1 for bad
+ *   arguments); wh_resample_workspace(rate_in) bytes of workspace hold the polyphase table
+ *   (built on the device by every call; 16-byte aligned).
+ *   x     device float32 [batch][n_in] at rate_in Hz, 1000 <= rate_in <= 384000
+ *   y     device float32 [batch][wh_resample_length(n_in, rate_in)] at 16 kHz
+ * Errors: WH_EINVAL, WH_ENOSPC, WH_ECUDA.  batch == 0 or n_in == 0 is a no-op.
+ * ------------------------------------------------------------------------------------ */
+int64_t wh_resample_length(int64_t n_in, int rate_in);
+size_t wh_resample_workspace(int rate_in);
+int wh_resample(const float *x, int64_t n_in, int batch, int rate_in, float *y, void *workspace,
+                size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
  * wh_frontend_static: wh_frontend for callers that cannot allocate device memory.
  * (The pages have no counterpart: this is an interface choice of this library.)
  * Some callers cannot hand the library a scratch buffer at the point they call in: a

@@ -280,3 +280,53 @@ def attend_one(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_head: int) -> np.n
         p = np.exp(s - s.max())
         out[sl] = (p / p.sum()) @ v[:, sl]
     return out
+
+
+# ========================================================================================
+# Upstream front end: 30-s windows of a long clip  [API] main.nu (wh_run); resampling to
+# 16 kHz with a windowed sinc  [README] "Transcribing", "How it is verified"
+# ========================================================================================
+def long_clip_windows(pcm: np.ndarray) -> list:
+    """A clip longer than 30 s is cut into consecutive 30-s windows ([API] main.nu, wh_run),
+    the last one zero-padded; each window is then an independent 480000-sample input."""
+    x = np.asarray(pcm, dtype=np.float32)
+    n_win = -(-x.shape[0] // N_SAMPLES)
+    out = []
+    for w in range(n_win):
+        seg = x[w * N_SAMPLES:(w + 1) * N_SAMPLES]
+        out.append(np.concatenate([seg, np.zeros(N_SAMPLES - seg.shape[0], np.float32)]))
+    return out
+
+
+def resample_to_16k(x: np.ndarray, rate_in: int) -> np.ndarray:
+    """Windowed-sinc resampling to 16 kHz (reading r21: resample_poly's default design, the
+    routine the pages check against).  With up / down = 16000 / rate_in in lowest terms and
+    M = max(up, down): a low-pass at 1/M of the upsampled Nyquist rate, f sinc(f (t - H)) with
+    f = 1/M, H = 10 M, t = 0 .. 2H, times a Kaiser window (beta 5), scaled to unit DC gain and
+    then by up.  The output is the zero-phase filtered, upsampled-by-up signal kept every
+    down-th sample:  y[j] = sum_i h[j down + H - i up] x[i],  j < ceil(n up / down)."""
+    from math import gcd
+    x = _f64(x)
+    g = gcd(16000, int(rate_in))
+    up, down = 16000 // g, int(rate_in) // g
+    m_rate = max(up, down)
+    half = 10 * m_rate
+    t = np.arange(2 * half + 1, dtype=np.float64)
+    f = 1.0 / m_rate
+    beta = 5.0
+    win = np.i0(beta * np.sqrt(np.clip(1.0 - ((t - half) / half) ** 2, 0.0, None))) / np.i0(beta)
+    lp = f * np.sinc(f * (t - half))
+    h = up * (win * lp) / np.sum(win * lp)
+    n = x.shape[0]
+    n_out = -(-n * up // down)
+    j = np.arange(n_out, dtype=np.int64)
+    m = j * down + half
+    y = np.zeros(n_out, dtype=np.float64)
+    # the sum over i, enumerated by the taps t = m - i up that fall inside the filter
+    i_hi = m // up
+    for k in range(-(-(2 * half + 1) // up) + 1):
+        i = i_hi - k
+        tap = m - i * up
+        ok = (i >= 0) & (i < n) & (tap <= 2 * half)
+        y[ok] += h[tap[ok]] * x[i[ok]]
+    return y

@@ -187,3 +187,22 @@ def test_decode_attention_rejects_bad_arguments(L):
     args = list(good)
     args[7] = 0
     assert L.wh_decode_attention(*args) == wh.WH_OK
+
+
+def test_long_clip_and_resample_argument_checks(L):
+    assert L.wh_frontend_windows(0) == 0 and L.wh_frontend_windows(1) == 1
+    assert L.wh_frontend_windows(480000) == 1 and L.wh_frontend_windows(480001) == 2
+    assert L.wh_frontend_long(FAKE, -1, 80, FAKE, FAKE, 1 << 20, None) == wh.WH_EINVAL
+    assert L.wh_frontend_long(FAKE, 480000, 81, FAKE, FAKE, 1 << 20, None) == wh.WH_EINVAL
+    assert L.wh_frontend_long(None, 480000, 80, FAKE, FAKE, 1 << 20, None) == wh.WH_EINVAL
+    assert L.wh_frontend_long(FAKE, 480000 * 70000, 80, FAKE, FAKE, 1 << 30, None) == wh.WH_EINVAL
+    assert L.wh_frontend_long(FAKE, 3 * 480000, 80, FAKE, FAKE, 4, None) == wh.WH_ENOSPC
+    assert L.wh_frontend_long(None, 0, 80, None, None, 0, None) == wh.WH_OK
+    assert L.wh_resample_length(44100, 44100) == 16000
+    assert L.wh_resample_length(1, 44100) == 1 and L.wh_resample_length(0, 8000) == 0
+    assert L.wh_resample_length(100, 999) == -1 and L.wh_resample_length(-1, 8000) == -1
+    assert L.wh_resample_workspace(999) == 0 and L.wh_resample_workspace(44100) >= 160 * 56 * 4
+    assert L.wh_resample(FAKE, 100, 1, 500, FAKE, FAKE, 1 << 20, None) == wh.WH_EINVAL
+    assert L.wh_resample(None, 100, 1, 44100, FAKE, FAKE, 1 << 20, None) == wh.WH_EINVAL
+    assert L.wh_resample(FAKE, 100, 1, 44100, FAKE, FAKE, 16, None) == wh.WH_ENOSPC
+    assert L.wh_resample(FAKE, 0, 1, 44100, FAKE, FAKE, 0, None) == wh.WH_OK

@@ -222,3 +222,48 @@ def test_decode_attention_repeated_calls_reuse_the_workspace():
         b = wh.wh_decode_attention(q, k, v, D, n * D, n, 20, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+# ---- upstream front end: resampling and long clips -------------------------------------------
+@pytest.mark.parametrize("rate", [44100, 48000, 22050, 8000, 11025, 32000, 16000, 16001])
+def test_resample_parity(rate):
+    rng = np.random.default_rng(rate + 1)
+    n = rate // 3 + 101
+    x = rng.standard_normal((2, n)).astype(np.float32)
+    y = wh.wh_resample(torch.from_numpy(x).cuda(), rate)
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    y = y.cpu().numpy()
+    for b in range(2):
+        ref = R.resample_to_16k(x[b], rate)
+        assert y[b].shape == ref.shape
+        err = float(np.max(np.abs(y[b] - ref)))
+        assert err <= 1e-5, f"rate {rate}: max |gpu - oracle| {err:.3e}"
+
+
+def test_long_clip_frontend_matches_its_windows():
+    """A 2.26-window clip: each 30-s window's log-mel equals the oracle's on that window
+    (zero-padded), and equals wh_frontend on the zero-padded batch bit for bit."""
+    cfg = configs.CONFIGS[2]
+    n = 2 * 480000 + 123457
+    pcm = np.concatenate([synth.waveform(cfg, i) for i in range(3)])[:n]
+    mel_long = wh.wh_frontend_long(torch.from_numpy(pcm).cuda(), cfg.n_mels)
+    windows = R.long_clip_windows(pcm)
+    mel_batch = wh.wh_frontend(torch.from_numpy(np.stack(windows)).cuda(), cfg.n_mels)
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    assert mel_long.shape == (3, 3000, cfg.n_mels)
+    assert torch.equal(mel_long, mel_batch)
+    got = mel_long.cpu().numpy()
+    for w in (1, 2):
+        ref = R.log_mel(windows[w], cfg.n_mels)
+        assert float(np.max(np.abs(got[w] - ref))) <= 1e-3
+
+
+def test_long_clip_frontend_edge_lengths():
+    x = torch.from_numpy(synth.waveform(configs.CONFIGS[0], 0)).cuda()
+    assert wh.wh_frontend_long(x[:0].contiguous(), 80).shape[0] == 0
+    one = wh.wh_frontend_long(x, 80)                              # exactly 480000 samples
+    ref = wh.wh_frontend(x[None].contiguous(), 80)
+    torch.cuda.synchronize()
+    assert one.shape[0] == 1 and torch.equal(one, ref)

@@ -141,3 +141,44 @@ def test_attend_one_matches_torch_sdpa():
     vt = torch.from_numpy(v).reshape(n, n_head, 64).permute(1, 0, 2)[None]
     ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt).reshape(-1).numpy()
     np.testing.assert_allclose(R.attend_one(q, k, v, n_head), ref, rtol=1e-10, atol=1e-12)
+
+
+# ---- upstream front end: long clips and resampling ------------------------------------------
+def test_long_clip_windows_cover_the_clip_and_pad_the_last():
+    x = np.arange(2 * 480000 + 1234, dtype=np.float32)
+    w = R.long_clip_windows(x)
+    assert len(w) == 3 and all(v.shape == (480000,) for v in w)
+    np.testing.assert_array_equal(np.concatenate(w)[: x.shape[0]], x)
+    assert np.all(w[2][1234:] == 0.0)
+    assert R.long_clip_windows(np.zeros(0, np.float32)) == []
+
+
+@pytest.mark.parametrize("rate", [44100, 48000, 22050, 8000, 11025, 32000, 24000])
+def test_resample_matches_scipy_resample_poly(rate):
+    signal = pytest.importorskip("scipy.signal")
+    from math import gcd
+    rng = np.random.default_rng(rate)
+    x = rng.standard_normal(rate // 4 + 37)
+    g = gcd(16000, rate)
+    ref = signal.resample_poly(x, 16000 // g, rate // g)
+    got = R.resample_to_16k(x, rate)
+    assert got.shape == ref.shape
+    np.testing.assert_allclose(got, ref, rtol=1e-9, atol=1e-10)
+
+
+def test_resample_at_16k_is_the_identity():
+    x = np.random.default_rng(1).standard_normal(5000)
+    np.testing.assert_allclose(R.resample_to_16k(x, 16000), x, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("rate", [44100, 8000])
+def test_resample_keeps_a_passband_tone(rate):
+    """A 1 kHz tone sampled at `rate` comes out as the same tone at 16 kHz (away from the
+    clip's ends, within the Kaiser-window filter's passband ripple)."""
+    n = rate // 2
+    x = np.cos(2 * np.pi * 1000.0 * np.arange(n) / rate)
+    y = R.resample_to_16k(x, rate)
+    j = np.arange(y.shape[0])
+    ref = np.cos(2 * np.pi * 1000.0 * j / 16000.0)
+    mid = slice(400, y.shape[0] - 400)
+    assert np.max(np.abs(y[mid] - ref[mid])) < 5e-3

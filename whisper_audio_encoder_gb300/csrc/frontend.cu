@@ -100,9 +100,12 @@ __device__ __forceinline__ float key2f(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-__global__ void __launch_bounds__(THREADS) k_logmel(const float *__restrict__ pcm, long long n, int n_mels,
-                                                    int table, float *__restrict__ mel,
-                                                    uint32_t *__restrict__ wmax) {
+// Window b starts at pcm + b * stride and holds min(n, total - b * stride) samples (a batch of
+// clips: stride = n, total = batch * n; one long clip cut into 30-s windows: stride = n =
+// 480000, total = the clip's length).
+__global__ void __launch_bounds__(THREADS) k_logmel(const float *__restrict__ pcm, long long n, long long stride,
+                                                    long long total, int n_mels, int table,
+                                                    float *__restrict__ mel, uint32_t *__restrict__ wmax) {
     extern __shared__ float4 smem4[];
     float *seg = reinterpret_cast<float *>(smem4);       // staged samples, then the power [FB][201]
     float2 *Z = reinterpret_cast<float2 *>(seg + SEGP);  // [FB][ZSTRIDE]
@@ -113,7 +116,8 @@ __global__ void __launch_bounds__(THREADS) k_logmel(const float *__restrict__ pc
     const int b = blockIdx.y;
     const int t0 = blockIdx.x * FB;
     const int nf = min(FB, N_FRAMES - t0);
-    const float *x = pcm + (long long)b * n;
+    const float *x = pcm + (long long)b * stride;
+    n = min(n, total - (long long)b * stride);
 
     // Stage samples 160 t0 - 200 ... (pad/truncate to 480000, then reflect by 200).  Blocks
     // whose span lies inside the clip and is 16-byte aligned copy with float4 loads.
@@ -337,11 +341,12 @@ int frontend_init_tables() {
     return WH_OK;
 }
 
-int frontend_launch(const float *pcm, int64_t n, int batch, int n_mels, float *mel, uint32_t *wmax,
-                    cudaStream_t s) {
+int frontend_launch(const float *pcm, int64_t n, int64_t stride, int64_t total, int batch, int n_mels, float *mel,
+                    uint32_t *wmax, cudaStream_t s) {
     if (cudaMemsetAsync(wmax, 0, sizeof(uint32_t) * (size_t)batch, s) != cudaSuccess) return WH_ECUDA;
     dim3 grid((N_FRAMES + FB - 1) / FB, batch);
-    k_logmel<<<grid, THREADS, SMEM, s>>>(pcm, (long long)n, n_mels, n_mels == 128 ? 1 : 0, mel, wmax);
+    k_logmel<<<grid, THREADS, SMEM, s>>>(pcm, (long long)n, (long long)stride, (long long)total, n_mels,
+                                         n_mels == 128 ? 1 : 0, mel, wmax);
     const int per4 = N_FRAMES * n_mels / 4;
     dim3 cgrid((per4 + 255) / 256, batch);
     k_clamp<<<cgrid, 256, 0, s>>>(reinterpret_cast<float4 *>(mel), per4, wmax);

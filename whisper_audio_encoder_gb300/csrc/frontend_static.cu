@@ -63,5 +63,5 @@ extern "C" int wh_frontend_static(const float *pcm, int64_t n, int batch, int n_
     uint32_t *scratch = nullptr;
     if (int rc = scratch_for_current_device(&scratch)) return rc;
     // frontend_launch clears the per-window maxima (cudaMemsetAsync) before its kernels run.
-    return frontend_launch(pcm, n, batch, n_mels, mel, scratch, static_cast<cudaStream_t>(stream));
+    return frontend_launch(pcm, n, n, n * batch, batch, n_mels, mel, scratch, static_cast<cudaStream_t>(stream));
 }

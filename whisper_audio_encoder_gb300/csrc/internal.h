@@ -41,7 +41,9 @@ int gemm_prepare(int num_sms);
 
 // ---- front end (frontend.cu) -------------------------------------------------------------
 int frontend_init_tables();   // once per device (current device)
-int frontend_launch(const float *pcm, int64_t n, int batch, int n_mels, float *mel, uint32_t *wmax,
+// window b: pcm + b * stride, min(n, total - b * stride) samples
+int frontend_launch(const float *pcm, int64_t n, int64_t stride, int64_t total, int batch, int n_mels, float *mel,
+                    uint32_t *wmax,
                     cudaStream_t s);
 
 // ---- other kernels ---------------------------------------------------------------------
@@ -50,6 +52,11 @@ int layernorm_launch(const float *x, int rows, int d, const float *g, const floa
 int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
                      int num_sms, cudaStream_t s);
 int attention_prepare();
+// windowed-sinc resampling to 16 kHz (resample.cu)
+bool resample_rate_ok(int rate_in);
+long long resample_length(long long n_in, int rate_in);
+size_t resample_workspace(int rate_in);
+int resample_launch(const float *x, long long n_in, int batch, int rate_in, float *y, void *table, cudaStream_t s);
 // one-query attention of a decoder step, keys split across blocks (decode_attention.cu)
 size_t decode_attention_workspace(int batch, int n_head, int max_keys);
 int decode_attention_launch(const void *q, const void *k, const void *v, long long row_stride, long long seq_stride,
@@ -69,7 +76,7 @@ int device_setup();
 // Kernel classes for the per-kernel timing.
 enum TraceClass {
     TR_FRONTEND = 0, TR_STEM_PREP, TR_GEMM, TR_ATTN, TR_LAYERNORM,
-    TR_GEMM_CONV, TR_GEMM_QKV, TR_GEMM_OUT, TR_GEMM_FC1, TR_GEMM_FC2, TR_CROSS_PREP, TR_GEMM_CROSS, TR_DEC_ATTN, TR_NCLASS
+    TR_GEMM_CONV, TR_GEMM_QKV, TR_GEMM_OUT, TR_GEMM_FC1, TR_GEMM_FC2, TR_CROSS_PREP, TR_GEMM_CROSS, TR_DEC_ATTN, TR_RESAMPLE, TR_NCLASS
 };
 void trace_begin(int cls, cudaStream_t s);
 void trace_end(int cls, cudaStream_t s, double flops, double bytes);

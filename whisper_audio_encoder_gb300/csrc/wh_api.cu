@@ -84,7 +84,7 @@ struct TraceRec {
 const char *const kTraceNames[TR_NCLASS] = {"frontend", "stem_prep", "gemm",       "attention",
                                              "layernorm", "gemm_conv", "gemm_qkv",   "gemm_out",
                                              "gemm_fc1",  "gemm_fc2",  "cross_prep", "gemm_cross",
-                                             "decode_attention"};
+                                             "decode_attention", "resample"};
 std::mutex g_tr_mu;
 bool g_tr_on = false;
 std::vector<TraceRec> g_tr;
@@ -241,9 +241,58 @@ int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel, 
     if (int rc = ensure_device(&st)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     trace_begin(TR_FRONTEND, s);
-    const int rc = frontend_launch(pcm, n, batch, n_mels, mel, static_cast<uint32_t *>(workspace), s);
+    const int rc = frontend_launch(pcm, n, n, n * batch, batch, n_mels, mel, static_cast<uint32_t *>(workspace), s);
     const double n_read = (double)(n < 480000 ? n : 480000);
     trace_end(TR_FRONTEND, s, 0.0, batch * (n_read * 4.0 + 3000.0 * n_mels * 4.0));
+    return rc;
+}
+
+int64_t wh_frontend_windows(int64_t n_total) {
+    return n_total <= 0 ? 0 : (n_total + (int64_t)N_FRAMES * 160 - 1) / ((int64_t)N_FRAMES * 160);
+}
+
+int wh_frontend_long(const float *pcm, int64_t n_total, int n_mels, float *mel, void *workspace, size_t ws_bytes,
+                     void *stream) {
+    if (n_total < 0 || (n_mels != 80 && n_mels != 128)) return WH_EINVAL;
+    const int64_t windows = wh_frontend_windows(n_total);
+    if (windows == 0) return WH_OK;
+    if (windows > 65535) return WH_EINVAL;
+    if (!pcm || !mel || !workspace || !aligned(pcm, 16) || !aligned(mel, 16) || !aligned(workspace, 16))
+        return WH_EINVAL;
+    if (ws_bytes < wh_frontend_workspace((int)windows)) return WH_ENOSPC;
+    DevState *st;
+    if (int rc = ensure_device(&st)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t win = (int64_t)N_FRAMES * 160;  // 480000 samples, 30 s
+    trace_begin(TR_FRONTEND, s);
+    const int rc = frontend_launch(pcm, win, win, n_total, (int)windows, n_mels, mel,
+                                   static_cast<uint32_t *>(workspace), s);
+    trace_end(TR_FRONTEND, s, 0.0, (double)n_total * 4.0 + (double)windows * N_FRAMES * n_mels * 4.0);
+    return rc;
+}
+
+int64_t wh_resample_length(int64_t n_in, int rate_in) {
+    if (n_in < 0 || !resample_rate_ok(rate_in)) return -1;
+    return resample_length(n_in, rate_in);
+}
+
+size_t wh_resample_workspace(int rate_in) {
+    if (!resample_rate_ok(rate_in)) return 0;
+    return up256(resample_workspace(rate_in));
+}
+
+int wh_resample(const float *x, int64_t n_in, int batch, int rate_in, float *y, void *workspace, size_t ws_bytes,
+                void *stream) {
+    if (n_in < 0 || batch < 0 || batch > 65535 || !resample_rate_ok(rate_in)) return WH_EINVAL;
+    if (batch == 0 || n_in == 0) return WH_OK;
+    if (!x || !y || !workspace || !aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 16)) return WH_EINVAL;
+    if (ws_bytes < wh_resample_workspace(rate_in)) return WH_ENOSPC;
+    DevState *st;
+    if (int rc = ensure_device(&st)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    trace_begin(TR_RESAMPLE, s);
+    const int rc = resample_launch(x, n_in, batch, rate_in, y, workspace, s);
+    trace_end(TR_RESAMPLE, s, 0.0, (double)batch * (n_in + resample_length(n_in, rate_in)) * 4.0);
     return rc;
 }
 

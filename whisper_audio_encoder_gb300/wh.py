@@ -78,6 +78,11 @@ def lib():
         "wh_decode_attention_workspace": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
         "wh_decode_attention": (ctypes.c_int, [_p, _p, _p, ctypes.c_int64, ctypes.c_int64, _p, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, _p, _p, ctypes.c_size_t, _p]),
+        "wh_frontend_windows": (ctypes.c_int64, [ctypes.c_int64]),
+        "wh_frontend_long": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int, _p, _p, ctypes.c_size_t, _p]),
+        "wh_resample_length": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int]),
+        "wh_resample_workspace": (ctypes.c_size_t, [ctypes.c_int]),
+        "wh_resample": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _p, _p, ctypes.c_size_t, _p]),
         "wh_layer_norm": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, _p, _p, _p, ctypes.c_int, _p]),
         "wh_linear": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, _p, ctypes.c_int, _p, ctypes.c_int, _p, _p]),
         "wh_attention": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _p, _p]),
@@ -140,6 +145,40 @@ def wh_frontend(pcm, n_mels: int, mel=None, workspace=None, stream=None):
                            _stream(stream))
     _check(rc, "wh_frontend")
     return mel
+
+
+def wh_frontend_long(pcm, n_mels: int, mel=None, workspace=None, stream=None):
+    """One long clip, float32 CUDA tensor [n] -> log-mel [ceil(n / 480000)][3000][n_mels]
+    (consecutive 30-s windows, the last zero-padded)."""
+    import torch
+    assert pcm.dtype == torch.float32 and pcm.dim() == 1 and pcm.is_contiguous()
+    n = pcm.shape[0]
+    windows = lib().wh_frontend_windows(n)
+    if mel is None:
+        mel = torch.empty(max(windows, 0), N_FRAMES, n_mels, dtype=torch.float32, device=pcm.device)
+    if workspace is None:
+        workspace = torch.empty(max(16, wh_frontend_workspace(max(windows, 1))), dtype=torch.uint8, device=pcm.device)
+    _check(lib().wh_frontend_long(_ptr(pcm), n, n_mels, _ptr(mel), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)), "wh_frontend_long")
+    return mel
+
+
+def wh_resample(x, rate_in: int, y=None, workspace=None, stream=None):
+    """x float32 CUDA tensor [batch][n] at rate_in Hz -> [batch][n_out] at 16 kHz."""
+    import torch
+    assert x.dtype == torch.float32 and x.dim() == 2 and x.is_contiguous()
+    batch, n = x.shape
+    n_out = lib().wh_resample_length(n, rate_in)
+    if n_out < 0:
+        raise WhError(WH_EINVAL, "wh_resample_length")
+    if y is None:
+        y = torch.empty(batch, n_out, dtype=torch.float32, device=x.device)
+    need = max(256, lib().wh_resample_workspace(rate_in))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _check(lib().wh_resample(_ptr(x), n, batch, rate_in, _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "wh_resample")
+    return y
 
 
 def wh_layer_norm(x, g, b, out_bf16=True, y=None, stream=None):
