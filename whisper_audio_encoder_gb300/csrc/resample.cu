@@ -14,7 +14,7 @@
 //
 // k_resample_table builds P on the device in float64 (S is summed once per rate on the host),
 // so a call records into a CUDA graph without host-to-device copies; k_resample computes one
-// output sample per thread (K fused multiply-adds; the inputs a warp needs are contiguous).
+// output sample per thread from a block-wide input span staged in shared memory.
 #include <cmath>
 #include <map>
 #include <mutex>
@@ -89,24 +89,40 @@ __global__ void k_resample_table(Plan pl, double inv_s, float *__restrict__ tabl
     }
 }
 
-__global__ void __launch_bounds__(256) k_resample(const float *__restrict__ x, long long n_in, Plan pl,
-                                                  const float *__restrict__ table, float *__restrict__ y,
-                                                  long long n_out) {
+// One block computes 256 consecutive outputs.  Their taps read one contiguous input span,
+// staged in shared memory first (zeros outside the clip), so the inner loop is a plain FMA
+// chain over the phase's K taps: xs[ihi - lo - k] * P[p][k].
+constexpr int RS_THREADS = 256;
+
+__global__ void __launch_bounds__(RS_THREADS) k_resample(const float *__restrict__ x, long long n_in, Plan pl,
+                                                         const float *__restrict__ table, float *__restrict__ y,
+                                                         long long n_out) {
+    extern __shared__ float xs[];
     const float *xb = x + (long long)blockIdx.y * n_in;
     float *yb = y + (long long)blockIdx.y * n_out;
-    for (long long j = blockIdx.x * (long long)blockDim.x + threadIdx.x; j < n_out;
-         j += (long long)gridDim.x * blockDim.x) {
-        const long long m = j * pl.down + pl.H;
-        const long long i_hi = m / pl.up;
-        const long long p = m - i_hi * pl.up;
-        const float *ph = table + p * pl.K;
-        float acc = 0.0f;
-        for (long long k = 0; k < pl.K; ++k) {
-            const long long i = i_hi - k;
-            if (i < 0) break;
-            if (i < n_in) acc = fmaf(__ldg(ph + k), __ldg(xb + i), acc);
+    const int K = (int)pl.K;
+    for (long long j0 = (long long)blockIdx.x * RS_THREADS; j0 < n_out; j0 += (long long)gridDim.x * RS_THREADS) {
+        const long long jl = j0 + RS_THREADS - 1 < n_out ? j0 + RS_THREADS - 1 : n_out - 1;
+        const long long ihi0 = (j0 * pl.down + pl.H) / pl.up, ihi1 = (jl * pl.down + pl.H) / pl.up;
+        const long long lo = ihi0 - (K - 1);
+        const int cnt = (int)(ihi1 - lo + 1);   // <= floor(255 down / up) + 1 + K (the launch's bound)
+        __syncthreads();                        // the previous tile's reads are done
+        for (int t = threadIdx.x; t < cnt; t += RS_THREADS) {
+            const long long i = lo + t;
+            xs[t] = (i >= 0 && i < n_in) ? __ldg(xb + i) : 0.0f;
         }
-        yb[j] = acc;
+        __syncthreads();
+        const long long j = j0 + threadIdx.x;
+        if (j < n_out) {
+            const long long m = j * pl.down + pl.H;
+            const long long ihi = m / pl.up;
+            const float *ph = table + (m - ihi * pl.up) * K;
+            const float *xp = xs + (ihi - lo);
+            float acc = 0.0f;
+#pragma unroll 4
+            for (int k = 0; k < K; ++k) acc = fmaf(__ldg(ph + k), xp[-k], acc);
+            yb[j] = acc;
+        }
     }
 }
 
@@ -146,8 +162,10 @@ int resample_launch(const float *x, long long n_in, int batch, int rate_in, floa
     k_resample_table<<<(unsigned)(tb < 4096 ? tb : 4096), 256, 0, s>>>(pl, 1.0 / S, static_cast<float *>(table));
     const long long n_out = resample_length(n_in, rate_in);
     if (n_out > 0) {
-        const long long blocks = (n_out + 255) / 256;
-        k_resample<<<dim3((unsigned)(blocks < 8192 ? blocks : 8192), batch), 256, 0, s>>>(
+        const long long blocks = (n_out + RS_THREADS - 1) / RS_THREADS;
+        const size_t span = (size_t)((RS_THREADS - 1) * pl.down / pl.up + 1 + pl.K + 1);
+        if (span * sizeof(float) > 48 * 1024) return WH_EINVAL;   // not reached for 1 kHz .. 384 kHz
+        k_resample<<<dim3((unsigned)(blocks < 8192 ? blocks : 8192), batch), RS_THREADS, span * sizeof(float), s>>>(
             x, n_in, pl, static_cast<const float *>(table), y, n_out);
         count_launch(2);
     } else {
