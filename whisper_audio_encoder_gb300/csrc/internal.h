@@ -56,7 +56,9 @@ int attention_prepare();
 bool resample_rate_ok(int rate_in);
 long long resample_length(long long n_in, int rate_in);
 size_t resample_workspace(int rate_in);
-int resample_launch(const float *x, long long n_in, int batch, int rate_in, float *y, void *table, cudaStream_t s);
+int resample_launch(const float *x, long long n_in, int batch, int rate_in, float *y, void *table, int num_sms,
+                    cudaStream_t s);
+int resample_prepare();
 // one-query attention of a decoder step, keys split across blocks (decode_attention.cu)
 size_t decode_attention_workspace(int batch, int n_head, int max_keys);
 int decode_attention_launch(const void *q, const void *k, const void *v, long long row_stride, long long seq_stride,

@@ -89,25 +89,41 @@ __global__ void k_resample_table(Plan pl, double inv_s, float *__restrict__ tabl
     }
 }
 
-// One block computes 256 consecutive outputs.  Their taps read one contiguous input span,
-// staged in shared memory first (zeros outside the clip), so the inner loop is a plain FMA
-// chain over the phase's K taps: xs[ihi - lo - k] * P[p][k].
+// A block computes tiles of 256 consecutive outputs.  Their taps read one contiguous input
+// span, staged in shared memory first (zeros outside the clip), so the inner loop is a plain
+// FMA chain over the phase's K taps: xs[ihi - lo - k] * P[p][k].  Consecutive outputs use
+// different phases, so when the table fits (SMEM_TABLE) the block first copies it into shared
+// memory with an odd row stride (lanes of a warp then hit distinct banks) and walks many
+// tiles; larger tables (input rates with few common factors with 16 kHz) are read through L1.
 constexpr int RS_THREADS = 256;
+constexpr size_t RS_TABLE_SMEM_MAX = 40 * 1024;
 
+template <bool SMEM_TABLE>
 __global__ void __launch_bounds__(RS_THREADS) k_resample(const float *__restrict__ x, long long n_in, Plan pl,
                                                          const float *__restrict__ table, float *__restrict__ y,
-                                                         long long n_out) {
-    extern __shared__ float xs[];
+                                                         long long n_out, int span) {
+    extern __shared__ float sm_rs[];
+    const int K = (int)pl.K;
+    const int ks = SMEM_TABLE ? (K | 1) : K;   // table row stride
+    float *tab = sm_rs;                        // [up][ks] when SMEM_TABLE
+    float *xs = sm_rs + (SMEM_TABLE ? (int)pl.up * ks : 0);
+    if (SMEM_TABLE) {
+        const int n = (int)pl.up * K;
+        for (int t = threadIdx.x; t < n; t += RS_THREADS) {
+            const int pp = t / K, kk = t - pp * K;
+            tab[pp * ks + kk] = __ldg(table + t);
+        }
+    }
+    const float *tp = SMEM_TABLE ? tab : table;
     const float *xb = x + (long long)blockIdx.y * n_in;
     float *yb = y + (long long)blockIdx.y * n_out;
-    const int K = (int)pl.K;
     for (long long j0 = (long long)blockIdx.x * RS_THREADS; j0 < n_out; j0 += (long long)gridDim.x * RS_THREADS) {
         const long long jl = j0 + RS_THREADS - 1 < n_out ? j0 + RS_THREADS - 1 : n_out - 1;
         const long long ihi0 = (j0 * pl.down + pl.H) / pl.up, ihi1 = (jl * pl.down + pl.H) / pl.up;
         const long long lo = ihi0 - (K - 1);
-        const int cnt = (int)(ihi1 - lo + 1);   // <= floor(255 down / up) + 1 + K (the launch's bound)
-        __syncthreads();                        // the previous tile's reads are done
-        for (int t = threadIdx.x; t < cnt; t += RS_THREADS) {
+        const int cnt = (int)(ihi1 - lo + 1);   // <= span (the launch's bound)
+        __syncthreads();                        // the table is in; the previous tile's reads are done
+        for (int t = threadIdx.x; t < cnt && t < span; t += RS_THREADS) {
             const long long i = lo + t;
             xs[t] = (i >= 0 && i < n_in) ? __ldg(xb + i) : 0.0f;
         }
@@ -116,15 +132,18 @@ __global__ void __launch_bounds__(RS_THREADS) k_resample(const float *__restrict
         if (j < n_out) {
             const long long m = j * pl.down + pl.H;
             const long long ihi = m / pl.up;
-            const float *ph = table + (m - ihi * pl.up) * K;
+            const float *ph = tp + (m - ihi * pl.up) * ks;
             const float *xp = xs + (ihi - lo);
             float acc = 0.0f;
 #pragma unroll 4
-            for (int k = 0; k < K; ++k) acc = fmaf(__ldg(ph + k), xp[-k], acc);
+            for (int k = 0; k < K; ++k) acc = fmaf(ph[k], xp[-k], acc);
             yb[j] = acc;
         }
     }
 }
+
+size_t table_smem_bytes(const Plan &pl) { return (size_t)pl.up * (size_t)(pl.K | 1) * sizeof(float); }
+size_t span_of(const Plan &pl) { return (size_t)((RS_THREADS - 1) * pl.down / pl.up + 1 + pl.K + 1); }
 
 std::mutex g_norm_mu;
 std::map<int, double> g_norm;   // S per input rate
@@ -154,23 +173,44 @@ size_t resample_workspace(int rate_in) {
     return (size_t)(pl.up * pl.K) * sizeof(float);
 }
 
-int resample_launch(const float *x, long long n_in, int batch, int rate_in, float *y, void *table, cudaStream_t s) {
+int resample_prepare() {
+    // the largest dynamic shared memory a launch below asks for: a 40 KB table + a 26.4 KB span
+    const int bytes = (int)(RS_TABLE_SMEM_MAX + 28 * 1024);
+    return (cudaFuncSetAttribute(k_resample<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+            cudaFuncSetAttribute(k_resample<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess)
+               ? WH_OK
+               : WH_ECUDA;
+}
+
+int resample_launch(const float *x, long long n_in, int batch, int rate_in, float *y, void *table, int num_sms,
+                    cudaStream_t s) {
     const Plan pl = plan_of(rate_in);
     const double S = norm_of(rate_in, pl);
     const long long nt = pl.up * pl.K;
     const long long tb = (nt + 255) / 256;
     k_resample_table<<<(unsigned)(tb < 4096 ? tb : 4096), 256, 0, s>>>(pl, 1.0 / S, static_cast<float *>(table));
     const long long n_out = resample_length(n_in, rate_in);
+    int launches = 1;
     if (n_out > 0) {
-        const long long blocks = (n_out + RS_THREADS - 1) / RS_THREADS;
-        const size_t span = (size_t)((RS_THREADS - 1) * pl.down / pl.up + 1 + pl.K + 1);
-        if (span * sizeof(float) > 48 * 1024) return WH_EINVAL;   // not reached for 1 kHz .. 384 kHz
-        k_resample<<<dim3((unsigned)(blocks < 8192 ? blocks : 8192), batch), RS_THREADS, span * sizeof(float), s>>>(
-            x, n_in, pl, static_cast<const float *>(table), y, n_out);
-        count_launch(2);
-    } else {
-        count_launch(1);
+        const long long tiles = (n_out + RS_THREADS - 1) / RS_THREADS;
+        const size_t span = span_of(pl);
+        if (span * sizeof(float) > 28 * 1024) return WH_EINVAL;   // not reached for 1 kHz .. 384 kHz
+        const bool smem_table = table_smem_bytes(pl) <= RS_TABLE_SMEM_MAX;
+        if (smem_table) {
+            // about two blocks per SM over the whole batch: each block copies the table once
+            long long per_clip = (2LL * num_sms + batch - 1) / batch;
+            if (per_clip > tiles) per_clip = tiles;
+            if (per_clip < 1) per_clip = 1;
+            k_resample<true><<<dim3((unsigned)per_clip, batch), RS_THREADS, table_smem_bytes(pl) + span * sizeof(float),
+                               s>>>(x, n_in, pl, static_cast<const float *>(table), y, n_out, (int)span);
+        } else {
+            k_resample<false><<<dim3((unsigned)(tiles < 8192 ? tiles : 8192), batch), RS_THREADS,
+                                span * sizeof(float), s>>>(x, n_in, pl, static_cast<const float *>(table), y, n_out,
+                                                          (int)span);
+        }
+        ++launches;
     }
+    count_launch(launches);
     return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
 }
 

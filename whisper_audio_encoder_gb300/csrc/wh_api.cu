@@ -58,6 +58,7 @@ int ensure_device(DevState **out) {
         if (int rc = frontend_init_tables()) return rc;
         if (int rc = gemm_prepare(st.num_sms)) return rc;
         if (int rc = attention_prepare()) return rc;
+        if (int rc = resample_prepare()) return rc;
         st.status = static_cast<int *>(p);
         st.ready = true;
     }
@@ -291,7 +292,7 @@ int wh_resample(const float *x, int64_t n_in, int batch, int rate_in, float *y, 
     if (int rc = ensure_device(&st)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     trace_begin(TR_RESAMPLE, s);
-    const int rc = resample_launch(x, n_in, batch, rate_in, y, workspace, s);
+    const int rc = resample_launch(x, n_in, batch, rate_in, y, workspace, st->num_sms, s);
     trace_end(TR_RESAMPLE, s, 0.0, (double)batch * (n_in + resample_length(n_in, rate_in)) * 4.0);
     return rc;
 }
