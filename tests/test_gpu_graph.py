@@ -41,3 +41,22 @@ def test_graph_replay_equals_direct_calls():
         assert np.array_equal(out.cpu().numpy(), ref)
     assert wh.wh_status() == wh.WH_OK
     graph.destroy()
+
+
+def test_pipeline_serves_batches_in_order():
+    """The double-buffered serving loop (wh.Pipeline) returns, for each of five batches, exactly
+    the memory a direct call gives for that batch, although copies and passes overlap."""
+    cfg = configs.CONFIGS[1]
+    enc = wh.Encoder(cfg, synth.weights(cfg))
+    B = cfg.batch
+    batches = [torch.from_numpy(synth.waveforms(cfg, windows=range(8 * k, 8 * k + B))).pin_memory()
+               for k in range(5)]
+    outs = [torch.empty(B, 1500, cfg.d_model).pin_memory() for _ in range(5)]
+    pipe = wh.Pipeline(enc, B, batches[0].shape[1])
+    pipe.run(batches, outs)
+    assert wh.wh_status() == wh.WH_OK
+    for k in range(5):
+        ref = enc.forward(batches[k].cuda()).cpu()
+        torch.cuda.synchronize()
+        assert torch.equal(outs[k], ref), f"batch {k}"
+    pipe.destroy()

@@ -437,3 +437,52 @@ class CrossKV:
                                     _ptr(self._ws), self._ws.numel(), _stream(stream))
         _check(rc, "wh_prepare_cross")
         return kv
+
+
+class Pipeline:
+    """A double-buffered serving loop over recorded passes.
+
+    Two device buffer sets, each with its own recorded front end + encoder pass (the
+    log-mel buffer and the encoder workspace are shared: the passes run one after the other
+    on the compute stream).  While batch k is encoded, batch k+1's PCM is copied in on one
+    copy stream and batch k-1's encoder memory is copied out on another; stream events keep
+    a buffer from being overwritten before the pass or copy that uses it has finished."""
+
+    def __init__(self, enc, batch: int, n_samples: int = N_SAMPLES):
+        import torch
+        dev = enc.device
+        self.enc = enc
+        self.compute = torch.cuda.Stream(dev)
+        self.copy_in = torch.cuda.Stream(dev)
+        self.copy_out = torch.cuda.Stream(dev)
+        self.mel = torch.empty(batch, N_FRAMES, enc.cfg.n_mels, dtype=torch.float32, device=dev)
+        self.pcm = [torch.empty(batch, n_samples, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.out = [torch.empty(batch, N_CTX, enc.cfg.d_model, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.graphs = [enc.capture(self.pcm[i], self.mel, self.out[i], self.compute) for i in range(2)]
+        self.in_done = [torch.cuda.Event() for _ in range(2)]
+        self.pass_done = [torch.cuda.Event() for _ in range(2)]
+        self.out_done = [torch.cuda.Event() for _ in range(2)]
+
+    def run(self, pcm_host, out_host):
+        """pcm_host / out_host: lists of pinned host tensors, one per batch; encodes them in
+        order and returns when every result is on the host."""
+        import torch
+        for k, (src, dst) in enumerate(zip(pcm_host, out_host)):
+            i = k & 1
+            self.copy_in.wait_event(self.pass_done[i])        # the pass that read pcm[i] is done
+            with torch.cuda.stream(self.copy_in):
+                self.pcm[i].copy_(src, non_blocking=True)
+            self.in_done[i].record(self.copy_in)
+            self.compute.wait_event(self.in_done[i])
+            self.compute.wait_event(self.out_done[i])         # out[i] has been copied out
+            self.graphs[i].launch(self.compute)
+            self.pass_done[i].record(self.compute)
+            self.copy_out.wait_event(self.pass_done[i])
+            with torch.cuda.stream(self.copy_out):
+                dst.copy_(self.out[i], non_blocking=True)
+            self.out_done[i].record(self.copy_out)
+        self.copy_out.synchronize()
+
+    def destroy(self):
+        for g in self.graphs:
+            g.destroy()
