@@ -225,6 +225,9 @@ typedef struct wh_graph wh_graph;
 int wh_graph_capture(const float *pcm, int64_t n, int batch, const wh_config *cfg, const wh_weights *w,
                      float *mel, float *out, void *fe_ws, size_t fe_ws_bytes, void *enc_ws, size_t enc_ws_bytes,
                      void *stream, wh_graph **graph);
+/* The encoder alone (wh_encode's arguments): mel is the recorded pass's input. */
+int wh_graph_capture_encode(const float *mel, int batch, const wh_config *cfg, const wh_weights *w,
+                            float *out, void *enc_ws, size_t enc_ws_bytes, void *stream, wh_graph **graph);
 int wh_graph_launch(wh_graph *graph, void *stream);
 int wh_graph_destroy(wh_graph *graph);
 

@@ -116,6 +116,10 @@ def test_graph_entry_points_reject_bad_arguments(L):
                               1 << 30, None, ctypes.byref(h)) == wh.WH_EINVAL          # default stream
     assert L.wh_graph_capture(FAKE, 480000, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, FAKE, 256, FAKE,
                               1 << 30, FAKE, None) == wh.WH_EINVAL                     # no graph slot
+    assert L.wh_graph_capture_encode(FAKE, 1, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 1 << 30, None,
+                                     ctypes.byref(h)) == wh.WH_EINVAL                  # default stream
+    assert L.wh_graph_capture_encode(FAKE, 0, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, 1 << 30, FAKE,
+                                     ctypes.byref(h)) == wh.WH_EINVAL                  # empty batch
     assert L.wh_graph_launch(None, None) == wh.WH_EINVAL
     assert L.wh_graph_destroy(None) == wh.WH_EINVAL
 

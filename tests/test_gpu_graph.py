@@ -60,3 +60,18 @@ def test_pipeline_serves_batches_in_order():
         torch.cuda.synchronize()
         assert torch.equal(outs[k], ref), f"batch {k}"
     pipe.destroy()
+
+
+def test_encoder_only_recording_equals_wh_encode():
+    cfg = configs.CONFIGS[1]
+    enc = wh.Encoder(cfg, synth.weights(cfg))
+    mel = wh.wh_frontend(torch.from_numpy(synth.waveforms(cfg)).cuda(), cfg.n_mels)
+    ref = enc.wh_encode(mel).clone()
+    out = torch.empty_like(ref)
+    torch.cuda.synchronize()          # the direct call and the recorded pass share one workspace
+    stream = torch.cuda.Stream()
+    g = enc.capture_encode(mel, out, stream)
+    g.launch(stream)
+    stream.synchronize()
+    assert torch.equal(out, ref)
+    g.destroy()

@@ -514,16 +514,11 @@ struct wh_graph {
     cudaGraphExec_t exec;
 };
 
-extern "C" {
+namespace {
 
-int wh_graph_capture(const float *pcm, int64_t n, int batch, const wh_config *cfg, const wh_weights *w, float *mel,
-                     float *out, void *fe_ws, size_t fe_ws_bytes, void *enc_ws, size_t enc_ws_bytes, void *stream,
-                     wh_graph **graph) {
-    if (!graph || !stream || batch <= 0) return WH_EINVAL;
-    *graph = nullptr;
-    DevState *st;
-    if (int rc = ensure_device(&st)) return rc;  // constant tables and kernel set-up, outside the capture
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// Records what `body` launches on `stream` into an instantiated graph (tracing off meanwhile).
+template <typename Body>
+int record_graph(cudaStream_t s, wh_graph **graph, Body body) {
     bool tracing;
     {
         std::lock_guard<std::mutex> lk(g_tr_mu);
@@ -532,11 +527,11 @@ int wh_graph_capture(const float *pcm, int64_t n, int batch, const wh_config *cf
     }
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
         cudaGetLastError();
+        std::lock_guard<std::mutex> lk(g_tr_mu);
         g_tr_on = tracing;
         return WH_ECUDA;
     }
-    int rc = wh_frontend(pcm, n, batch, cfg ? cfg->n_mels : 0, mel, fe_ws, fe_ws_bytes, stream);
-    if (rc == WH_OK) rc = wh_encode(mel, batch, cfg, w, out, enc_ws, enc_ws_bytes, stream);
+    const int rc = body();
     cudaGraph_t g = nullptr;
     const cudaError_t ec = cudaStreamEndCapture(s, &g);
     {
@@ -556,6 +551,34 @@ int wh_graph_capture(const float *pcm, int64_t n, int batch, const wh_config *cf
     }
     *graph = new wh_graph{g, e};
     return WH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wh_graph_capture(const float *pcm, int64_t n, int batch, const wh_config *cfg, const wh_weights *w, float *mel,
+                     float *out, void *fe_ws, size_t fe_ws_bytes, void *enc_ws, size_t enc_ws_bytes, void *stream,
+                     wh_graph **graph) {
+    if (!graph || !stream || batch <= 0) return WH_EINVAL;
+    *graph = nullptr;
+    DevState *st;
+    if (int rc = ensure_device(&st)) return rc;  // constant tables and kernel set-up, outside the capture
+    return record_graph(static_cast<cudaStream_t>(stream), graph, [&]() {
+        int rc = wh_frontend(pcm, n, batch, cfg ? cfg->n_mels : 0, mel, fe_ws, fe_ws_bytes, stream);
+        if (rc == WH_OK) rc = wh_encode(mel, batch, cfg, w, out, enc_ws, enc_ws_bytes, stream);
+        return rc;
+    });
+}
+
+int wh_graph_capture_encode(const float *mel, int batch, const wh_config *cfg, const wh_weights *w, float *out,
+                            void *enc_ws, size_t enc_ws_bytes, void *stream, wh_graph **graph) {
+    if (!graph || !stream || batch <= 0) return WH_EINVAL;
+    *graph = nullptr;
+    DevState *st;
+    if (int rc = ensure_device(&st)) return rc;
+    return record_graph(static_cast<cudaStream_t>(stream), graph,
+                        [&]() { return wh_encode(mel, batch, cfg, w, out, enc_ws, enc_ws_bytes, stream); });
 }
 
 int wh_graph_launch(wh_graph *graph, void *stream) {

@@ -95,6 +95,9 @@ def lib():
         "wh_graph_capture": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int, ctypes.POINTER(wh_config),
                                             ctypes.POINTER(wh_weights), _p, _p, _p, ctypes.c_size_t, _p,
                                             ctypes.c_size_t, _p, ctypes.POINTER(ctypes.c_void_p)]),
+        "wh_graph_capture_encode": (ctypes.c_int, [_p, ctypes.c_int, ctypes.POINTER(wh_config),
+                                                   ctypes.POINTER(wh_weights), _p, _p, ctypes.c_size_t, _p,
+                                                   ctypes.POINTER(ctypes.c_void_p)]),
         "wh_graph_launch": (ctypes.c_int, [_p, _p]),
         "wh_graph_destroy": (ctypes.c_int, [_p]),
     }
@@ -360,6 +363,16 @@ class Encoder:
                                     ctypes.byref(h))
         _check(rc, "wh_graph_capture")
         return Graph(h, (pcm, mel, out, ws, fe))
+
+    def capture_encode(self, mel, out, stream):
+        """Records one wh_encode pass (mel -> memory) over these device buffers."""
+        batch = mel.shape[0]
+        ws = self.workspace(batch)
+        h = ctypes.c_void_p()
+        rc = lib().wh_graph_capture_encode(_ptr(mel), batch, ctypes.byref(self.c_cfg), ctypes.byref(self.c_w), _ptr(out),
+                                           _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(h))
+        _check(rc, "wh_graph_capture_encode")
+        return Graph(h, (mel, out, ws))
 
     def encode_from_host(self, pcm_host, out_host, pcm_dev, mel, out_dev, stream=None):
         """End to end from pinned host memory: copy PCM in, front end + encoder, copy the
