@@ -293,6 +293,13 @@ int wh_decode_attention(const wh_bf16 *q, const wh_bf16 *k, const wh_bf16 *v, in
  * WH_OK, WH_ETIMEOUT or WH_EBOUNDS (or WH_ECUDA if the synchronisation failed). */
 int wh_status(void *stream);
 
+/* Forgets the library's per-device set-up (kernel attributes, status-word address, the
+ * constant tables' "ready" mark) and its host-side caches; the next call on a device sets it
+ * up again.  The constant tables are static device arrays: nothing is freed, nothing the
+ * caller owns is touched, and no device is reset.  Call it with no call of this library in
+ * flight (after a stream synchronisation). */
+int wh_shutdown(void);
+
 /* A static, NUL-terminated name for a WH_* code. */
 const char *wh_strerror(int code);
 

@@ -210,3 +210,10 @@ def test_long_clip_and_resample_argument_checks(L):
     assert L.wh_resample(None, 100, 1, 44100, FAKE, FAKE, 1 << 20, None) == wh.WH_EINVAL
     assert L.wh_resample(FAKE, 100, 1, 44100, FAKE, FAKE, 16, None) == wh.WH_ENOSPC
     assert L.wh_resample(FAKE, 0, 1, 44100, FAKE, FAKE, 0, None) == wh.WH_OK
+
+
+def test_shutdown_forgets_state_and_the_library_sets_up_again(L):
+    assert L.wh_shutdown() == wh.WH_OK
+    assert L.wh_shutdown() == wh.WH_OK                       # idempotent
+    if not torch.cuda.is_available():
+        assert L.wh_frontend(FAKE, 480000, 1, 80, FAKE, FAKE, 256, None) == wh.WH_ENODEV

@@ -75,3 +75,15 @@ def test_encoder_only_recording_equals_wh_encode():
     stream.synchronize()
     assert torch.equal(out, ref)
     g.destroy()
+
+
+def test_calls_after_shutdown_set_the_device_up_again():
+    cfg = configs.CONFIGS[0]
+    x = torch.from_numpy(synth.waveforms(cfg)).cuda()
+    a = wh.wh_frontend(x, cfg.n_mels).clone()
+    torch.cuda.synchronize()
+    assert wh.lib().wh_shutdown() == wh.WH_OK
+    b = wh.wh_frontend(x, cfg.n_mels)
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    assert torch.equal(a, b)

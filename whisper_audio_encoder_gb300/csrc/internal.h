@@ -59,6 +59,7 @@ size_t resample_workspace(int rate_in);
 int resample_launch(const float *x, long long n_in, int batch, int rate_in, float *y, void *table, int num_sms,
                     cudaStream_t s);
 int resample_prepare();
+void resample_forget();   // drops the per-rate filter normalisers (wh_shutdown)
 // one-query attention of a decoder step, keys split across blocks (decode_attention.cu)
 size_t decode_attention_workspace(int batch, int n_head, int max_keys);
 int decode_attention_launch(const void *q, const void *k, const void *v, long long row_stride, long long seq_stride,

@@ -161,6 +161,11 @@ double norm_of(int rate_in, const Plan &pl) {
 
 }  // namespace
 
+void resample_forget() {
+    std::lock_guard<std::mutex> lk(g_norm_mu);
+    g_norm.clear();
+}
+
 bool resample_rate_ok(int rate_in) { return rate_in >= 1000 && rate_in <= 384000; }
 
 long long resample_length(long long n_in, int rate_in) {

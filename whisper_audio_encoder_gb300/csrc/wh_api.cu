@@ -229,6 +229,15 @@ const char *wh_strerror(int code) {
 
 int64_t wh_launch_count(void) { return g_launches.exchange(0); }
 
+int wh_shutdown(void) {
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        for (DevState &st : g_dev) st = DevState();
+    }
+    resample_forget();
+    return WH_OK;
+}
+
 size_t wh_frontend_workspace(int batch) { return batch <= 0 ? 0 : up256(sizeof(uint32_t) * (size_t)batch); }
 
 int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel, void *workspace, size_t ws_bytes,

@@ -88,6 +88,7 @@ def lib():
         "wh_attention": (ctypes.c_int, [_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _p, _p]),
         "wh_status": (ctypes.c_int, [_p]),
         "wh_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "wh_shutdown": (ctypes.c_int, []),
         "wh_selftest_timeout": (ctypes.c_int, [ctypes.c_uint64, _p]),
         "wh_trace_enable": (ctypes.c_int, [ctypes.c_int]),
         "wh_trace_read": (ctypes.c_int, [ctypes.POINTER(wh_trace_stat), ctypes.c_int]),
