@@ -202,8 +202,9 @@ int resample_launch(const float *x, long long n_in, int batch, int rate_in, floa
         if (span * sizeof(float) > 28 * 1024) return WH_EINVAL;   // not reached for 1 kHz .. 384 kHz
         const bool smem_table = table_smem_bytes(pl) <= RS_TABLE_SMEM_MAX;
         if (smem_table) {
-            // about two blocks per SM over the whole batch: each block copies the table once
-            long long per_clip = (2LL * num_sms + batch - 1) / batch;
+            // about four blocks per SM over the whole batch (each copies the table once; up to
+            // 40 + 28 KB of shared memory per block leaves room for four)
+            long long per_clip = (4LL * num_sms + batch - 1) / batch;
             if (per_clip > tiles) per_clip = tiles;
             if (per_clip < 1) per_clip = 1;
             k_resample<true><<<dim3((unsigned)per_clip, batch), RS_THREADS, table_smem_bytes(pl) + span * sizeof(float),
