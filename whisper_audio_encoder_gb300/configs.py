@@ -4,8 +4,9 @@ Shapes follow the Whisper family table of "How Audio Becomes Words: Whisper's Ke
 Step By Step On A CPU" (section "Tiny, Base, Small, Large: What Actually Changes"):
 tiny 4 layers / 384 / 6 heads, base 6 / 512 / 8, small 12 / 768 / 12, large 32 / 1280 / 20
 with 128 mel bins for large-v3.  The feed-forward width is 4 * d_model (the same page,
-section "The Full Stitched Circuit": "mlp_up d to 4d").  The first workload is a one-block
-tiny-width encoder, the smallest case that still runs every kernel of the path.
+section "The Full Stitched Circuit", where the MLP widens d to four times d).  The first
+workload is a one-block tiny-width encoder, the smallest case that still runs every kernel
+of the path.
 """
 from dataclasses import dataclass, field
 
@@ -46,7 +47,7 @@ class EncoderConfig:
 
 
 CONFIGS = [
-    EncoderConfig("pr1-tiny-width-1block", 80, 384, 6, 1, 1536, 1, "sines", index=0),
+    EncoderConfig("tiny-width-1block", 80, 384, 6, 1, 1536, 1, "sines", index=0),
     EncoderConfig("whisper-tiny", 80, 384, 6, 4, 1536, 8, "sines", silent_windows=(0, 1), index=1),
     EncoderConfig("whisper-base", 80, 512, 8, 6, 2048, 16, "speech", index=2),
     EncoderConfig("whisper-small", 80, 768, 12, 12, 3072, 32, "speech", index=3),
