@@ -12,8 +12,13 @@ Sources (web pages the method is described on; section names as they appear ther
             the bullets that walk them), "The Encoder: Understand Once",
             "The Full Stitched Circuit", "Tiny, Base, Small, Large".
   [API]  "whisper 0.9.0 API" -- model.nu (encoder shape, k_proj without bias, wh_encode
-         layouts) and kernels.nu (LayerNorm with bias, erf GELU, conv1d, non-causal
-         attention with the 1/sqrt(hd) score scale).
+         layouts, wh_prepare_cross, wh_decode_step), kernels.nu (LayerNorm with bias, erf
+         GELU, conv1d, non-causal attention with the 1/sqrt(hd) score scale) and main.nu
+         (long audio in 30-s windows).
+  [README] the "whisper" package page -- "Serving" (draft encoder over a shorter context),
+         "Transcribing" and "How it is verified" (windowed-sinc resampling to 16 kHz,
+         checked against resample_poly), "Performance and memory" (one-query attention with
+         the keys split across blocks).
 
 Readings where the pages are silent (each is a decision, recorded with the code):
   r1  3000 frames: centred, reflect-padded frames t = 0..2999 (the 3001st is dropped).
@@ -30,6 +35,10 @@ Readings where the pages are silent (each is a decision, recorded with the code)
   r11 GELU is the exact erf form.
   r12 scores scaled by 1/sqrt(64); head h owns columns [64 h, 64 h + 64).
   r13 GELU after each conv; positions added after conv2's GELU.
+  r20 a shorter encoder context reads the first 2 n_ctx frames and zero-pads at their end.
+  r21 the windowed-sinc resampler is resample_poly's default design (Kaiser beta 5, 10 M
+      taps on each side, unit DC gain).
+  r22 long clips are cut into consecutive, non-overlapping 30-s windows, the last padded.
 
 Pinned by tests/test_oracle_*.py against closed forms, invariants, library routines
 (numpy.fft, torch.stft, torch.nn.functional) and brute force.  The full encoder has no
@@ -135,7 +144,7 @@ def log_mel_from_power(power: np.ndarray, fb: np.ndarray) -> np.ndarray:
 
 def log_mel(pcm: np.ndarray, n_mels: int) -> np.ndarray:
     """One window: pcm (any length, 16 kHz) -> log-mel float32 [3000][n_mels], a frame
-    contiguous ([API] wh_encode: 'mel is 3000 x n_mels, row-major')."""
+    contiguous (the layout [API] gives for wh_encode's input)."""
     x = pad_or_truncate(np.asarray(pcm, dtype=np.float64))
     p = dft_power(frame_signal(x), hann_periodic())
     return log_mel_from_power(p, mel_filterbank(n_mels)).astype(np.float32)
