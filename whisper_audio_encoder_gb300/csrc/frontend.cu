@@ -4,13 +4,21 @@
 // power re^2 + im^2 on the 201 x 3000 grid, Slaney area-normalised mel filters, log10,
 // clamp at (window maximum - 8) and (x + 4) / 4.
 //
-// Kernel 1 (k_logmel): one block = 30 consecutive frames of one window.  The 5040 samples
-// the frames touch are staged once in shared memory (coalesced; reflect and zero-extension
-// applied while loading).  Each real 400-point frame x is transformed as one complex
-// 200-point FFT of z[m] = x[2m] + i x[2m+1] (decomposed 200 = 8 x 25, the 25-point part as
-// 5 x 5), then split into the real spectrum X[k] = E[k] + W400^k O[k], k = 0..200.  The
-// power spectrum stays in shared memory; the sparse mel projection, log10 and the block's
-// maximum follow; one atomicMax per block builds the per-window maximum.
+// Kernel 1 (k_logmel): one block = a tile of 32 consecutive frames of one window, one frame
+// per lane.  The 5360 samples the tile touches are staged once in shared memory (coalesced;
+// reflect and zero-extension applied while loading), two pad floats after every 160 samples
+// so that the 32 frames' rows start in distinct banks.  Each real 400-point frame x is
+// transformed as the complex 200-point FFT of z[m] = w[2m] x[2m] + i w[2m+1] x[2m+1] (w the
+// Hann window), split by the prime-factor (Good-Thomas) map 200 = 8 x 25: with
+// m = (25 n1 + 8 n2) mod 200 and k = (25 k1 + 176 k2) mod 200,
+//   Z[k] = sum_n2 W25^(n2 k2) sum_n1 W8^(n1 k1) z[m],
+// i.e. 8-point DFTs over n1 then 25-point DFTs (5 x 5) over n2, with no twiddles between the
+// two (8 and 25 are coprime).  The real spectrum X[k] = E[k] + W400^k O[k] (E, O the spectra
+// of the even and odd samples) and its power follow, two mirrored bins (k, 200 - k) at a
+// time; then the sparse mel projection, log10 and the tile's maximum; one atomicMax per block
+// builds the per-window maximum.  Every stage keeps lanes on frames and the warp on one
+// index of the transform, so shared-memory accesses are conflict-free and the constant
+// tables (window, gather offsets, W400^k, mel filters) are read at warp-uniform addresses.
 // Kernel 2 (k_clamp): mel = (max(mel, g - 8) + 4) / 4 in place with the window maximum g.
 // Both read/write only the PCM and the log-mel (the intermediates never reach HBM).
 #include <cmath>
@@ -25,70 +33,201 @@ namespace wh {
 namespace {
 
 constexpr int N_FFT = 400, HOP = 160, N_FRAMES = 3000, N_SAMPLES = 480000, N_BINS = 201;
-constexpr int FB = 30;                          // frames per block: 3000 = 100 x 30
+constexpr int TF = 32;                            // frames per tile: one per lane
 constexpr int THREADS = 256;
-constexpr int SEG = FB * HOP + (N_FFT - HOP);   // 5040 staged samples
-constexpr int ZSTRIDE = 200;                    // complex slots per frame
-constexpr int MAXW = 512;                       // mel filter nonzeros (<= 2 per bin)
-// The staged samples are dead after stage A, so the power spectrum reuses their space.
-constexpr int SEGP = SEG > FB * N_BINS ? SEG : FB * N_BINS;
-constexpr size_t SMEM = (size_t)SEGP * 4 + (size_t)FB * ZSTRIDE * 8;
+constexpr int NWARP = THREADS / 32;
+constexpr int N1 = 8, N2 = 25;                    // 200 = N1 x N2
+constexpr int SPAN = TF * HOP + (N_FFT - HOP);    // 5360 samples a tile touches
+constexpr int ROW = HOP + 2;                      // staged floats per frame row
+// Staged sample j of the span sits at j + 2 floor(j / 160).
+__host__ __device__ constexpr int seg_pos(int j) { return j + 2 * (j / HOP); }
+constexpr int SEG_FLOATS = seg_pos(SPAN - 1) + 2;
+constexpr int P_ROWS = N_BINS - 2;                // bins 1 .. 199 (no mel filter touches 0 or 200)
+constexpr int P_FLOATS = P_ROWS * TF;
+constexpr int R1_FLOATS = SEG_FLOATS > P_FLOATS ? SEG_FLOATS : P_FLOATS;
+constexpr int R2_FLOAT2 = N1 * N2 * TF;           // the 200-point spectra of the tile
+constexpr int MT_STRIDE = 129;                    // log-mel tile row (odd: conflict-free)
+constexpr int MAXW = 512;                         // mel filter nonzeros (<= 2 per bin)
+constexpr size_t SMEM = (size_t)R1_FLOATS * 4 + (size_t)R2_FLOAT2 * 8;
+constexpr int A_TABLE = (SEG_FLOATS + 3) / 4 * 4;  // stage-A table above the staged samples
+static_assert(A_TABLE + N2 * 24 <= R1_FLOATS, "stage-A table must fit beside the samples");
+static_assert(TF * MT_STRIDE <= 2 * R2_FLOAT2, "log-mel tile must fit the spectrum region");
+static_assert((R1_FLOATS * 4) % 16 == 0, "spectrum region alignment");
 
-__device__ float g_hann[N_FFT];
-__device__ float2 g_tw[N_FFT];          // W400^j = (cos, -sin)(2 pi j / 400)
-__device__ int g_mel_start[2][128];     // first nonzero bin of filter m
-__device__ int g_mel_len[2][128];       // number of nonzero bins
-__device__ int g_mel_off[2][128];       // offset of its weights in g_mel_w
-__device__ float g_mel_w[2][MAXW];
+// Per n2, for n1 = 0 .. 7 and m = (25 n1 + 8 n2) mod 200: the Hann window pair (w[2m], w[2m+1])
+// and the staged offset of sample 2m within a frame row.
+struct ARow {
+    float2 w[8];
+    int off[8];
+};
+__constant__ ARow c_arow[N2];
+__constant__ float2 c_tw[101];          // W400^k = (cos, -sin)(2 pi k / 400), k = 0 .. 100
+__constant__ int c_mel_start[2][128];   // first nonzero bin of filter m
+__constant__ int c_mel_len[2][128];     // number of nonzero bins
+__constant__ int c_mel_off[2][128];     // offset of its weights in c_mel_w
+__constant__ float c_mel_w[2][MAXW];    // filter weights / 4 (the power is kept x 4)
 
-__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
-__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
-__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
-    return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
+// ---- compile-time shape of the transform and of the mel filters ------------------------
+// Staged offset (within a frame row) of sample 2m for z index m = (25 n1 + 8 n2) mod 200.
+__host__ __device__ constexpr int a_off(int n1, int n2) { return seg_pos(2 * ((25 * n1 + 8 * n2) % 200)); }
+
+// Natural exp and log in double by their series, evaluated by the compiler: the Slaney mel
+// filter edges (hz <-> mel) below, and from them which FFT bins each filter covers, so that
+// the kernel's mel projection is straight-line code.  (The weights themselves are built on
+// the host and read from c_mel_w; frontend_init_tables checks that both agree on the shape.)
+constexpr double kLn2 = 0.69314718055994530942;
+constexpr double ct_exp(double x) {   // exp(k ln2 + r) = 2^k exp(r), |r| <= ln2 / 2, Taylor
+    int k = (int)(x / kLn2 + (x >= 0.0 ? 0.5 : -0.5));
+    const double r = x - k * kLn2;
+    double term = 1.0, sum = 1.0;
+    for (int i = 1; i < 30; ++i) {
+        term *= r / i;
+        sum += term;
+    }
+    for (; k > 0; --k) sum *= 2.0;
+    for (; k < 0; ++k) sum *= 0.5;
+    return sum;
 }
-__device__ __forceinline__ float2 mul_negi(float2 a) { return make_float2(a.y, -a.x); }  // -i * a
-
-// 4-point DFT (W4 = -i).
-__device__ __forceinline__ void dft4(float2 &a0, float2 &a1, float2 &a2, float2 &a3) {
-    const float2 t0 = cadd(a0, a2), t1 = csub(a0, a2), t2 = cadd(a1, a3), t3 = csub(a1, a3);
-    a0 = cadd(t0, t2);
-    a2 = csub(t0, t2);
-    a1 = cadd(t1, mul_negi(t3));
-    a3 = csub(t1, mul_negi(t3));
+constexpr double ct_log(double x) {   // x = 2^e y, y in [1, 2): ln y = 2 atanh((y - 1) / (y + 1))
+    int e = 0;
+    while (x >= 2.0) {
+        x *= 0.5;
+        ++e;
+    }
+    while (x < 1.0) {
+        x *= 2.0;
+        --e;
+    }
+    const double z = (x - 1.0) / (x + 1.0), z2 = z * z;
+    double p = z, sum = 0.0;
+    for (int i = 0; i < 40; ++i) {
+        sum += p / (2 * i + 1);
+        p *= z2;
+    }
+    return 2.0 * sum + e * kLn2;
+}
+constexpr double ct_hz_to_mel(double f) {
+    return f < 1000.0 ? 3.0 * f / 200.0 : 15.0 + 27.0 * ct_log(f / 1000.0) / ct_log(6.4);
+}
+constexpr double ct_mel_to_hz(double m) {
+    return m < 15.0 ? 200.0 * m / 3.0 : 1000.0 * ct_exp((m - 15.0) * ct_log(6.4) / 27.0);
 }
 
-// 8-point DFT in place: two 4-point DFTs of the even and odd samples, then W8 twiddles.
-__device__ __forceinline__ void dft8(float2 (&a)[8]) {
-    float2 e0 = a[0], e1 = a[2], e2 = a[4], e3 = a[6];
-    float2 o0 = a[1], o1 = a[3], o2 = a[5], o3 = a[7];
-    dft4(e0, e1, e2, e3);
-    dft4(o0, o1, o2, o3);
-    const float r = 0.70710678118654752f;
-    o1 = make_float2(r * (o1.x + o1.y), r * (o1.y - o1.x));      // * (r, -r)
-    o2 = mul_negi(o2);                                           // * (0, -1)
-    o3 = make_float2(r * (o3.y - o3.x), -r * (o3.x + o3.y));     // * (-r, -r)
-    a[0] = cadd(e0, o0); a[4] = csub(e0, o0);
-    a[1] = cadd(e1, o1); a[5] = csub(e1, o1);
-    a[2] = cadd(e2, o2); a[6] = csub(e2, o2);
-    a[3] = cadd(e3, o3); a[7] = csub(e3, o3);
+// Filter m covers the bins k with f_m < 40 k < f_(m+2) (f_i the i-th of NM + 2 edges equally
+// spaced in mel from 0 to 8 kHz); its weights sit at c_mel_w[..][off[m] ...].
+template <int NM>
+struct MelShape {
+    int start[NM], len[NM], off[NM];
+    constexpr MelShape() : start(), len(), off() {
+        const double top = ct_hz_to_mel(8000.0);
+        int used = 0;
+        for (int m = 0; m < NM; ++m) {
+            const double lo = ct_mel_to_hz(top * m / (NM + 1)), hi = ct_mel_to_hz(top * (m + 2) / (NM + 1));
+            int k0 = -1, k1 = -1;
+            for (int k = 0; k < N_BINS; ++k) {
+                const double fk = 40.0 * k;
+                if (fk > lo && fk < hi) {
+                    if (k0 < 0) k0 = k;
+                    k1 = k;
+                }
+            }
+            start[m] = k0;
+            len[m] = k0 < 0 ? 0 : k1 - k0 + 1;
+            off[m] = used;
+            used += len[m];
+        }
+    }
+};
+template <int NM>
+struct Mel {
+    static constexpr MelShape<NM> shape{};
+};
+
+// 8-point DFT of u[n] = (w[n].x x[n].x, w[n].y x[n].y), the window folded into the first
+// radix-2 layer (n, n + 4).  Even outputs are the 4-point DFT of the sums, odd outputs the
+// 4-point DFT of the differences times W8^n.
+__device__ __forceinline__ void dft8_windowed(const float2 (&x)[8], const float2 *w, float2 (&X)[8]) {
+    float2 s[4], d[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 wa = w[j], wb = w[j + 4];
+        const float ar = wa.x * x[j].x, ai = wa.y * x[j].y;
+        s[j] = make_float2(fmaf(wb.x, x[j + 4].x, ar), fmaf(wb.y, x[j + 4].y, ai));
+        d[j] = make_float2(fmaf(-wb.x, x[j + 4].x, ar), fmaf(-wb.y, x[j + 4].y, ai));
+    }
+    const float h = 0.70710678118654752f;
+    {
+        const float2 p = make_float2(s[0].x + s[2].x, s[0].y + s[2].y), q = make_float2(s[0].x - s[2].x, s[0].y - s[2].y);
+        const float2 r = make_float2(s[1].x + s[3].x, s[1].y + s[3].y), t = make_float2(s[1].x - s[3].x, s[1].y - s[3].y);
+        X[0] = make_float2(p.x + r.x, p.y + r.y);
+        X[4] = make_float2(p.x - r.x, p.y - r.y);
+        X[2] = make_float2(q.x + t.y, q.y - t.x);   // q - i t
+        X[6] = make_float2(q.x - t.y, q.y + t.x);   // q + i t
+    }
+    {
+        const float2 e1 = make_float2(h * (d[1].x + d[1].y), h * (d[1].y - d[1].x));    // W8 d1
+        const float2 e2 = make_float2(d[2].y, -d[2].x);                                // W8^2 d2
+        const float2 e3 = make_float2(h * (d[3].y - d[3].x), -h * (d[3].x + d[3].y));   // W8^3 d3
+        const float2 p = make_float2(d[0].x + e2.x, d[0].y + e2.y), q = make_float2(d[0].x - e2.x, d[0].y - e2.y);
+        const float2 r = make_float2(e1.x + e3.x, e1.y + e3.y), t = make_float2(e1.x - e3.x, e1.y - e3.y);
+        X[1] = make_float2(p.x + r.x, p.y + r.y);
+        X[5] = make_float2(p.x - r.x, p.y - r.y);
+        X[3] = make_float2(q.x + t.y, q.y - t.x);
+        X[7] = make_float2(q.x - t.y, q.y + t.x);
+    }
 }
 
-// 5-point DFT of (y0..y4) with W5 = exp(-2 pi i / 5):
-//   X1,4 = y0 + c1 t1 + c2 t2 -/+ i (s1 t3 + s2 t4),  X2,3 = y0 + c2 t1 + c1 t2 -/+ i (s2 t3 - s1 t4)
-// with t1 = y1 + y4, t2 = y2 + y3, t3 = y1 - y4, t4 = y2 - y3.
+// 5-point DFT in place, W5 = exp(-2 pi i / 5), with t1 = y1 + y4, t2 = y2 + y3,
+// t3 = y1 - y4, t4 = y2 - y3:
+//   Y0 = y0 + t1 + t2,
+//   Y1, Y4 = y0 + c1 t1 + c2 t2 -/+ i (s1 t3 + s2 t4),
+//   Y2, Y3 = y0 + c2 t1 + c1 t2 -/+ i (s2 t3 - s1 t4),
+// c1, s1 = cos, sin (2 pi / 5) and c2, s2 = cos, sin (4 pi / 5).
 __device__ __forceinline__ void dft5(float2 &y0, float2 &y1, float2 &y2, float2 &y3, float2 &y4) {
-    const float c1 = 0.30901699437494742f, c2 = -0.80901699437494742f;
-    const float s1 = 0.95105651629515357f, s2 = 0.58778525229247313f;
-    const float2 t1 = cadd(y1, y4), t2 = cadd(y2, y3), t3 = csub(y1, y4), t4 = csub(y2, y3);
+    const float c1 = 0.30901699437494745f, c2 = -0.80901699437494734f;
+    const float s1 = 0.95105651629515353f, s2 = 0.58778525229247325f;
+    const float2 t1 = make_float2(y1.x + y4.x, y1.y + y4.y), t2 = make_float2(y2.x + y3.x, y2.y + y3.y);
+    const float2 t3 = make_float2(y1.x - y4.x, y1.y - y4.y), t4 = make_float2(y2.x - y3.x, y2.y - y3.y);
     const float2 a = make_float2(y0.x + c1 * t1.x + c2 * t2.x, y0.y + c1 * t1.y + c2 * t2.y);
-    const float2 b = make_float2(y0.x + c2 * t1.x + c1 * t2.x, y0.y + c2 * t1.y + c1 * t2.y);
+    const float2 c = make_float2(y0.x + c2 * t1.x + c1 * t2.x, y0.y + c2 * t1.y + c1 * t2.y);
     const float2 u = make_float2(s1 * t3.x + s2 * t4.x, s1 * t3.y + s2 * t4.y);
-    const float2 w = make_float2(s2 * t3.x - s1 * t4.x, s2 * t3.y - s1 * t4.y);
+    const float2 v = make_float2(s2 * t3.x - s1 * t4.x, s2 * t3.y - s1 * t4.y);
     y0 = make_float2(y0.x + t1.x + t2.x, y0.y + t1.y + t2.y);
-    y1 = cadd(a, mul_negi(u));
-    y4 = csub(a, mul_negi(u));
-    y2 = cadd(b, mul_negi(w));
-    y3 = csub(b, mul_negi(w));
+    y1 = make_float2(a.x + u.y, a.y - u.x);   // a - i u
+    y4 = make_float2(a.x - u.y, a.y + u.x);   // a + i u
+    y2 = make_float2(c.x + v.y, c.y - v.x);
+    y3 = make_float2(c.x - v.y, c.y + v.x);
+}
+
+// 25-point DFT in place, n = 5 a + b, k = c + 5 e: 5-point DFTs over a (for each b), the
+// twiddles W25^(b c), 5-point DFTs over b (for each c).  On return v[5 c + e] = X[c + 5 e].
+__device__ __forceinline__ void dft25(float2 (&v)[25]) {
+    // (cos, sin)(2 pi j / 25), j = 1 .. 16
+    constexpr float C[16] = {0.96858316112863108f, 0.87630668004386358f, 0.72896862742141155f,
+                             0.53582679497899655f, 0.30901699437494745f, 0.062790519529313527f,
+                             -0.1873813145857246f, -0.42577929156507272f, -0.63742398974868975f,
+                             -0.80901699437494734f, -0.92977648588825135f, -0.99211470131447776f,
+                             -0.99211470131447788f, -0.92977648588825146f, -0.80901699437494778f,
+                             -0.63742398974868952f};
+    constexpr float S[16] = {0.24868988716485479f, 0.48175367410171532f, 0.68454710592868862f,
+                             0.84432792550201508f, 0.95105651629515353f, 0.99802672842827156f,
+                             0.98228725072868872f, 0.90482705246601947f, 0.77051324277578925f,
+                             0.58778525229247325f, 0.36812455268467814f, 0.12533323356430454f,
+                             -0.12533323356430429f, -0.36812455268467792f, -0.58778525229247269f,
+                             -0.77051324277578936f};
+#pragma unroll
+    for (int b = 0; b < 5; ++b) dft5(v[b], v[5 + b], v[10 + b], v[15 + b], v[20 + b]);
+    // now v[5 c + b] = U[b][c]; multiply by W25^(b c) = (cos, -sin)(2 pi b c / 25)
+#pragma unroll
+    for (int b = 1; b < 5; ++b)
+#pragma unroll
+        for (int c = 1; c < 5; ++c) {
+            const float cs = C[b * c - 1], sn = S[b * c - 1];
+            const float2 a = v[5 * c + b];
+            v[5 * c + b] = make_float2(a.x * cs + a.y * sn, a.y * cs - a.x * sn);
+        }
+#pragma unroll
+    for (int c = 0; c < 5; ++c) dft5(v[5 * c], v[5 * c + 1], v[5 * c + 2], v[5 * c + 3], v[5 * c + 4]);
 }
 
 // Order-preserving map float -> uint32 (for atomicMax over signed floats).
@@ -100,159 +239,206 @@ __device__ __forceinline__ float key2f(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+// Stage A: frame = lane, n2 = warp, warp + 8, ...: the 8-point DFT over n1 of the windowed
+// z[(25 n1 + 8 n2) mod 200], stored at [k1][n2][frame].  The window pairs and gather offsets
+// of each n2 come from a small table in shared memory (one broadcast read per value).
+__device__ __forceinline__ void stage_a(const float *__restrict__ xf, const ARow *__restrict__ at,
+                                        float2 *__restrict__ R2, int warp, int lane) {
+    for (int n2 = warp; n2 < N2; n2 += NWARP) {
+        const ARow *r = at + n2;
+        float2 u[8], y[8], w[8];
+#pragma unroll
+        for (int n1 = 0; n1 < 8; ++n1) {
+            w[n1] = r->w[n1];
+            u[n1] = *reinterpret_cast<const float2 *>(xf + r->off[n1]);
+        }
+        dft8_windowed(u, w, y);
+        float2 *dst = R2 + n2 * TF + lane;
+#pragma unroll
+        for (int k1 = 0; k1 < 8; ++k1) dst[k1 * N2 * TF] = y[k1];
+    }
+}
+
+// Stage C: frame = lane, bin pairs (k, 200 - k) with k = warp + 8 i in 1 .. 100.  Z[k] sits at
+// [k mod 8][k mod 25].  With A = Z[k], B = Z[200 - k]: 2E = A + conj B, 2O = -i (A - conj B),
+// X[k] = E + W400^k O, X[200 - k] = conj(E - W400^k O).  The powers are kept x 4 (c_mel_w
+// carries the 1/4); bins 0 and 200 are not stored.
+__device__ __forceinline__ void stage_c(const float2 *__restrict__ R2, float *__restrict__ P, int warp, int lane) {
+    const float2 *za = R2 + warp * N2 * TF + lane;                  // k mod 8 = warp
+    const float2 *zb = R2 + ((8 - warp) & 7) * N2 * TF + lane;      // (200 - k) mod 8
+    int k = warp == 0 ? NWARP : warp;
+    int ka = k % 25;                                                // k mod 25
+    for (; k <= 100; k += NWARP) {
+        const int kb = ka == 0 ? 0 : 25 - ka;                       // (200 - k) mod 25
+        const float2 A = za[ka * TF];
+        const float2 B = zb[kb * TF];
+        const float er = A.x + B.x, ei = A.y - B.y;
+        const float o_r = A.y + B.y, o_i = B.x - A.x;
+        const float2 w = c_tw[k];
+        const float vr = w.x * o_r - w.y * o_i, vi = w.x * o_i + w.y * o_r;
+        const float pr = er + vr, pi = ei + vi, mr = er - vr, mi = ei - vi;
+        P[(k - 1) * TF + lane] = pr * pr + pi * pi;
+        P[(199 - k) * TF + lane] = mr * mr + mi * mi;   // bin 200 - k
+        ka = ka + 8 >= 25 ? ka + 8 - 25 : ka + 8;
+    }
+}
+
+// Stage D for warp W: frame = lane, filters m = W + 8 j: the sparse projection (straight-line:
+// bins and weight offsets are compile-time), log10 with floor 1e-10, into the log-mel tile
+// [frame][m]; the running maximum over valid frames.
+template <int NM, int W, int J>
+__device__ __forceinline__ void stage_d(const float *__restrict__ P, float *__restrict__ Mt, int lane, bool valid,
+                                        float &lmax) {
+    constexpr int m = W + NWARP * J;
+    if constexpr (m < NM) {
+        constexpr int T = NM == 128 ? 1 : 0;
+        constexpr int k0 = Mel<NM>::shape.start[m] - 1, len = Mel<NM>::shape.len[m], off = Mel<NM>::shape.off[m];
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < len; ++i) acc = fmaf(c_mel_w[T][off + i], P[(k0 + i) * TF + lane], acc);
+        // log10 via the hardware log2 (log10 x = log2 x * log10 2); at the floor exactly -10.
+        float lg2;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg2) : "f"(acc));
+        const float lg = acc > 1e-10f ? lg2 * 0.30102999566398120f : -10.0f;
+        Mt[lane * MT_STRIDE + m] = lg;
+        lmax = fmaxf(lmax, valid ? lg : -INFINITY);
+        stage_d<NM, W, J + 1>(P, Mt, lane, valid, lmax);
+    }
+}
+
+#define WH_WARP_SWITCH(call_w)                                                                       \
+    switch (warp) {                                                                                  \
+        case 0: call_w(0); break;                                                                    \
+        case 1: call_w(1); break;                                                                    \
+        case 2: call_w(2); break;                                                                    \
+        case 3: call_w(3); break;                                                                    \
+        case 4: call_w(4); break;                                                                    \
+        case 5: call_w(5); break;                                                                    \
+        case 6: call_w(6); break;                                                                    \
+        default: call_w(7); break;                                                                   \
+    }
+
 // Window b starts at pcm + b * stride and holds min(n, total - b * stride) samples (a batch of
 // clips: stride = n, total = batch * n; one long clip cut into 30-s windows: stride = n =
 // 480000, total = the clip's length).
-__global__ void __launch_bounds__(THREADS) k_logmel(const float *__restrict__ pcm, long long n, long long stride,
-                                                    long long total, int n_mels, int table,
-                                                    float *__restrict__ mel, uint32_t *__restrict__ wmax) {
+template <int NM>
+__global__ void __launch_bounds__(THREADS, 3) k_logmel(const float *__restrict__ pcm, long long n, long long stride,
+                                                       long long total, float *__restrict__ mel,
+                                                       uint32_t *__restrict__ wmax) {
     extern __shared__ float4 smem4[];
-    float *seg = reinterpret_cast<float *>(smem4);       // staged samples, then the power [FB][201]
-    float2 *Z = reinterpret_cast<float2 *>(seg + SEGP);  // [FB][ZSTRIDE]
-    float *P = seg;
-    __shared__ float red[THREADS / 32];
+    float *R1 = reinterpret_cast<float *>(smem4);             // staged samples, then the power [bin - 1][frame]
+    float2 *R2 = reinterpret_cast<float2 *>(R1 + R1_FLOATS);  // spectra [k1][k2][frame], then the log-mel tile
+    __shared__ float red[NWARP];
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.y;
-    const int t0 = blockIdx.x * FB;
-    const int nf = min(FB, N_FRAMES - t0);
+    const int t0 = blockIdx.x * TF;
+    const int nf = min(TF, N_FRAMES - t0);
     const float *x = pcm + (long long)b * stride;
     n = min(n, total - (long long)b * stride);
 
-    // Stage samples 160 t0 - 200 ... (pad/truncate to 480000, then reflect by 200).  Blocks
+    // The stage-A table (window pairs and gather offsets per n2) goes into the slack above the
+    // staged samples.
+    {
+        const int4 *src = reinterpret_cast<const int4 *>(c_arow);
+        int4 *dst = reinterpret_cast<int4 *>(R1 + A_TABLE);
+        for (int i = tid; i < (int)(sizeof(c_arow) / 16); i += THREADS) dst[i] = src[i];
+    }
+
+    // Stage samples 160 t0 - 200 ... (pad/truncate to 480000, then reflect by 200).  Tiles
     // whose span lies inside the clip and is 16-byte aligned copy with float4 loads.
     const long long s0 = (long long)HOP * t0 - N_FFT / 2;
     const long long lim = n < N_SAMPLES ? n : N_SAMPLES;
-    if (s0 >= 0 && s0 + SEG <= lim && ((reinterpret_cast<uintptr_t>(x + s0) & 15) == 0)) {
+    if (s0 >= 0 && s0 + SPAN <= lim && ((reinterpret_cast<uintptr_t>(x + s0) & 15) == 0)) {
         const float4 *src = reinterpret_cast<const float4 *>(x + s0);
-        float4 *dst = reinterpret_cast<float4 *>(seg);
-        for (int j = tid; j < SEG / 4; j += THREADS) dst[j] = __ldg(src + j);
+        for (int q = tid; q < SPAN / 4; q += THREADS) {
+            const float4 v = __ldg(src + q);
+            float *d = R1 + seg_pos(4 * q);   // the four samples share a row (160 % 4 == 0)
+            *reinterpret_cast<float2 *>(d) = make_float2(v.x, v.y);
+            *reinterpret_cast<float2 *>(d + 2) = make_float2(v.z, v.w);
+        }
     } else {
-        for (int j = tid; j < SEG; j += THREADS) {
-            int si = (int)s0 + j;
+        for (int j = tid; j < SPAN; j += THREADS) {
+            long long si = s0 + j;
             si = si < 0 ? -si : si;
-            si = si > N_SAMPLES - 1 ? 2 * (N_SAMPLES - 1) - si : si;
-            seg[j] = (si < n) ? __ldg(x + si) : 0.0f;
+            si = si > N_SAMPLES - 1 ? 2LL * (N_SAMPLES - 1) - si : si;
+            R1[seg_pos(j)] = (si < n) ? __ldg(x + si) : 0.0f;
         }
     }
     __syncthreads();
 
-    // Stage A: for each frame f and n2 in 0..24, the 8-point DFT over n1 of z[25 n1 + n2]
-    // (z[m] = w[2m] x[2m] + i w[2m+1] x[2m+1]), times W200^(n2 k1); stored as Z[f][25 k1 + n2].
-    for (int it = tid; it < nf * 25; it += THREADS) {
-        const int f = it / 25, n2 = it - f * 25;
-        const float *xf = seg + f * HOP;
-        float2 a[8];
-#pragma unroll
-        for (int n1 = 0; n1 < 8; ++n1) {
-            const int m = 25 * n1 + n2;
-            a[n1] = make_float2(g_hann[2 * m] * xf[2 * m], g_hann[2 * m + 1] * xf[2 * m + 1]);
-        }
-        dft8(a);
-        float2 *zf = Z + f * ZSTRIDE;
-        zf[n2] = a[0];
-#pragma unroll
-        for (int k1 = 1; k1 < 8; ++k1) zf[25 * k1 + n2] = cmul(a[k1], g_tw[2 * n2 * k1]);
-    }
+    stage_a(R1 + ROW * lane, reinterpret_cast<const ARow *>(R1 + A_TABLE), R2, warp, lane);
     __syncthreads();
 
-    // Stage B: for each frame f and k1 in 0..7, the 25-point DFT over n2 (n2 = 5a + b,
-    // k2 = c + 5e): 5-point DFTs over a, twiddles W25^(b c), 5-point DFTs over b.
-    // Output Z200[k1 + 8 k2] is written back in natural order after a block barrier.
-    float2 y[25];
-    int fB = -1, k1B = 0;
+    // Stage B: frame = lane, k1 = warp: the 25-point DFT over n2, in place;
+    // [k1][k2][frame] then holds Z[(25 k1 + 176 k2) mod 200].
     {
-        const int it = tid;  // nf * 8 <= 256 items: one per thread
-        if (it < nf * 8) {
-            fB = it >> 3;
-            k1B = it & 7;
-            const float2 *col = Z + fB * ZSTRIDE + 25 * k1B;
+        float2 *col = R2 + warp * N2 * TF + lane;
+        float2 v[25];
 #pragma unroll
-            for (int i = 0; i < 25; ++i) y[i] = col[i];
-#pragma unroll
-            for (int bb = 0; bb < 5; ++bb) dft5(y[bb], y[5 + bb], y[10 + bb], y[15 + bb], y[20 + bb]);
-            // now y[5 c + bb] = U[bb][c]
-#pragma unroll
-            for (int bb = 1; bb < 5; ++bb)
-#pragma unroll
-                for (int c = 1; c < 5; ++c) y[5 * c + bb] = cmul(y[5 * c + bb], g_tw[16 * bb * c]);
-#pragma unroll
-            for (int c = 0; c < 5; ++c) dft5(y[5 * c], y[5 * c + 1], y[5 * c + 2], y[5 * c + 3], y[5 * c + 4]);
-            // now y[5 c + e] = Z25[c + 5 e]
-        }
-    }
-    __syncthreads();
-    if (fB >= 0) {
-        float2 *zf = Z + fB * ZSTRIDE;
+        for (int i = 0; i < 25; ++i) v[i] = col[i * TF];
+        dft25(v);
 #pragma unroll
         for (int c = 0; c < 5; ++c)
 #pragma unroll
-            for (int e = 0; e < 5; ++e) zf[k1B + 8 * (c + 5 * e)] = y[5 * c + e];
+            for (int e = 0; e < 5; ++e) col[(c + 5 * e) * TF] = v[5 * c + e];
     }
     __syncthreads();
 
-    // Stage C: real spectrum and power, one warp per frame, lanes over bins.
-    // E = (Z[k] + conj Z[-k]) / 2, O = -i (Z[k] - conj Z[-k]) / 2, X[k] = E + W400^k O, P = |X|^2.
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int f = warp; f < nf; f += THREADS / 32) {
-        const float2 *zf = Z + f * ZSTRIDE;
-        float *pf = P + f * N_BINS;
-        for (int k = lane; k < N_BINS; k += 32) {
-            const float2 zk = zf[k == 200 ? 0 : k];
-            const float2 zm = zf[k == 0 ? 0 : 200 - k];
-            const float2 e = make_float2(0.5f * (zk.x + zm.x), 0.5f * (zk.y - zm.y));
-            const float2 o = make_float2(0.5f * (zk.y + zm.y), -0.5f * (zk.x - zm.x));
-            const float2 X = cadd(e, cmul(g_tw[k], o));
-            pf[k] = X.x * X.x + X.y * X.y;
-        }
-    }
+    float *P = R1;
+    stage_c(R2, P, warp, lane);
     __syncthreads();
 
-    // Stage D: mel projection, log10 with floor 1e-10, frame-major store, block maximum.
-    // One warp per frame, lanes over mel bins (coalesced stores).
     float lmax = -INFINITY;
-    const int *mstart = g_mel_start[table], *mlen = g_mel_len[table], *moff = g_mel_off[table];
-    const float *mw = g_mel_w[table];
-    for (int f = warp; f < nf; f += THREADS / 32) {
-        const float *pf = P + f * N_BINS;
-        float *out = mel + ((long long)b * N_FRAMES + t0 + f) * n_mels;
-        for (int m = lane; m < n_mels; m += 32) {
-            const int k0 = mstart[m], len = mlen[m];
-            const float *wm = mw + moff[m];
-            float acc = 0.0f;
-            for (int i = 0; i < len; ++i) acc = fmaf(wm[i], pf[k0 + i], acc);
-            // log10 via the hardware log2 (log10 x = log2 x * log10 2); at the floor exactly -10.
-            float lg2;
-            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg2) : "f"(acc));
-            const float lg = acc > 1e-10f ? lg2 * 0.30102999566398120f : -10.0f;
-            out[m] = lg;
-            lmax = fmaxf(lmax, lg);
-        }
+    float *Mt = reinterpret_cast<float *>(R2);
+    const bool valid = lane < nf;
+#define WH_STAGE_D(w) stage_d<NM, w, 0>(P, Mt, lane, valid, lmax)
+    WH_WARP_SWITCH(WH_STAGE_D)
+#undef WH_STAGE_D
+    __syncthreads();
+
+    // Frame-major store: one row of NM per frame, lanes over m (coalesced).
+    float *out = mel + ((long long)b * N_FRAMES + t0) * NM;
+    for (int f = warp; f < nf; f += NWARP) {
+#pragma unroll
+        for (int m0 = 0; m0 < NM; m0 += 32)
+            if (m0 + lane < NM) out[(long long)f * NM + m0 + lane] = Mt[f * MT_STRIDE + m0 + lane];
     }
+
     lmax = warp_max(lmax);
     if (lane == 0) red[warp] = lmax;
     __syncthreads();
     if (tid < 32) {
-        float v = tid < THREADS / 32 ? red[tid] : -INFINITY;
+        float v = tid < NWARP ? red[tid] : -INFINITY;
         v = warp_max(v);
         if (tid == 0) atomicMax(wmax + b, f2key(v));
     }
 }
+#undef WH_WARP_SWITCH
 
-// grid.y = window: mel[b] = (max(mel[b], g_b - 8) + 4) / 4, float4 at a time.
+// grid (x, window b): mel[b] = (max(mel[b], g_b - 8) + 4) / 4 in place, g_b the window
+// maximum; each thread clamps CL_PER float4 (all loads issued before the stores).
+constexpr int CL_PER = 4;
 __global__ void __launch_bounds__(256) k_clamp(float4 *__restrict__ mel, int per_window4,
                                                const uint32_t *__restrict__ wmax) {
     const int b = blockIdx.y;
-    const float floor = key2f(wmax[b]) - 8.0f;
+    const float floor = key2f(__ldg(wmax + b)) - 8.0f;
     float4 *w = mel + (long long)b * per_window4;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < per_window4; i += gridDim.x * blockDim.x) {
-        float4 v = w[i];
-        v.x = (fmaxf(v.x, floor) + 4.0f) * 0.25f;
-        v.y = (fmaxf(v.y, floor) + 4.0f) * 0.25f;
-        v.z = (fmaxf(v.z, floor) + 4.0f) * 0.25f;
-        v.w = (fmaxf(v.w, floor) + 4.0f) * 0.25f;
-        w[i] = v;
-    }
+    const int base = blockIdx.x * (256 * CL_PER) + threadIdx.x;
+    float4 v[CL_PER];
+#pragma unroll
+    for (int u = 0; u < CL_PER; ++u)
+        if (base + u * 256 < per_window4) v[u] = w[base + u * 256];
+#pragma unroll
+    for (int u = 0; u < CL_PER; ++u)
+        if (base + u * 256 < per_window4) {
+            float4 t = v[u];
+            t.x = (fmaxf(t.x, floor) + 4.0f) * 0.25f;
+            t.y = (fmaxf(t.y, floor) + 4.0f) * 0.25f;
+            t.z = (fmaxf(t.z, floor) + 4.0f) * 0.25f;
+            t.w = (fmaxf(t.w, floor) + 4.0f) * 0.25f;
+            w[base + u * 256] = t;
+        }
 }
 
 // ---- host-side constant tables (built in double precision) ----------------------------
@@ -304,13 +490,19 @@ int build_mel(int n_mels, MelTable &t) {
 }  // namespace
 
 int frontend_init_tables() {
-    float hann[N_FFT];
-    float2 tw[N_FFT];
     const double pi = 3.14159265358979323846;
-    for (int j = 0; j < N_FFT; ++j) {
-        hann[j] = (float)(0.5 - 0.5 * std::cos(2.0 * pi * j / N_FFT));
-        tw[j] = make_float2((float)std::cos(2.0 * pi * j / N_FFT), (float)-std::sin(2.0 * pi * j / N_FFT));
-    }
+    double hann[N_FFT];
+    for (int j = 0; j < N_FFT; ++j) hann[j] = 0.5 - 0.5 * std::cos(2.0 * pi * j / N_FFT);
+    ARow arow[N2];
+    for (int n2 = 0; n2 < N2; ++n2)
+        for (int n1 = 0; n1 < N1; ++n1) {
+            const int m = (25 * n1 + 8 * n2) % 200;
+            arow[n2].w[n1] = make_float2((float)hann[2 * m], (float)hann[2 * m + 1]);
+            arow[n2].off[n1] = a_off(n1, n2);
+        }
+    float2 tw[101];
+    for (int k = 0; k <= 100; ++k)
+        tw[k] = make_float2((float)std::cos(2.0 * pi * k / N_FFT), (float)-std::sin(2.0 * pi * k / N_FFT));
     static MelTable mt[2];
     static std::once_flag once;
     static int build_rc = WH_OK;
@@ -326,17 +518,28 @@ int frontend_init_tables() {
             start[t][m] = mt[t].start[m];
             len[t][m] = mt[t].len[m];
             off[t][m] = mt[t].off[m];
+            // the kernel stores the power of bins 1 .. 199 only and unrolls each filter over the
+            // bins its compile-time shape names: both must hold for the table built here
+            const int nm = t ? 128 : 80;
+            if (m < nm) {
+                if (start[t][m] < 1 || start[t][m] + len[t][m] - 1 > N_BINS - 2) return WH_EINVAL;
+                const int cs = t ? Mel<128>::shape.start[m] : Mel<80>::shape.start[m];
+                const int cl = t ? Mel<128>::shape.len[m] : Mel<80>::shape.len[m];
+                const int co = t ? Mel<128>::shape.off[m] : Mel<80>::shape.off[m];
+                if (cs != start[t][m] || cl != len[t][m] || co != off[t][m]) return WH_EINVAL;
+            }
         }
-        for (int i = 0; i < MAXW; ++i) w[t][i] = mt[t].w[i];
+        for (int i = 0; i < MAXW; ++i) w[t][i] = 0.25f * mt[t].w[i];
     }
-    if (cudaMemcpyToSymbol(g_hann, hann, sizeof(hann)) != cudaSuccess ||
-        cudaMemcpyToSymbol(g_tw, tw, sizeof(tw)) != cudaSuccess ||
-        cudaMemcpyToSymbol(g_mel_start, start, sizeof(start)) != cudaSuccess ||
-        cudaMemcpyToSymbol(g_mel_len, len, sizeof(len)) != cudaSuccess ||
-        cudaMemcpyToSymbol(g_mel_off, off, sizeof(off)) != cudaSuccess ||
-        cudaMemcpyToSymbol(g_mel_w, w, sizeof(w)) != cudaSuccess)
+    if (cudaMemcpyToSymbol(c_arow, arow, sizeof(arow)) != cudaSuccess ||
+        cudaMemcpyToSymbol(c_tw, tw, sizeof(tw)) != cudaSuccess ||
+        cudaMemcpyToSymbol(c_mel_start, start, sizeof(start)) != cudaSuccess ||
+        cudaMemcpyToSymbol(c_mel_len, len, sizeof(len)) != cudaSuccess ||
+        cudaMemcpyToSymbol(c_mel_off, off, sizeof(off)) != cudaSuccess ||
+        cudaMemcpyToSymbol(c_mel_w, w, sizeof(w)) != cudaSuccess)
         return WH_ECUDA;
-    if (cudaFuncSetAttribute(k_logmel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(k_logmel<80>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(k_logmel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) != cudaSuccess)
         return WH_ECUDA;
     return WH_OK;
 }
@@ -344,11 +547,13 @@ int frontend_init_tables() {
 int frontend_launch(const float *pcm, int64_t n, int64_t stride, int64_t total, int batch, int n_mels, float *mel,
                     uint32_t *wmax, cudaStream_t s) {
     if (cudaMemsetAsync(wmax, 0, sizeof(uint32_t) * (size_t)batch, s) != cudaSuccess) return WH_ECUDA;
-    dim3 grid((N_FRAMES + FB - 1) / FB, batch);
-    k_logmel<<<grid, THREADS, SMEM, s>>>(pcm, (long long)n, (long long)stride, (long long)total, n_mels,
-                                         n_mels == 128 ? 1 : 0, mel, wmax);
+    const dim3 grid((N_FRAMES + TF - 1) / TF, batch);
+    if (n_mels == 128)
+        k_logmel<128><<<grid, THREADS, SMEM, s>>>(pcm, (long long)n, (long long)stride, (long long)total, mel, wmax);
+    else
+        k_logmel<80><<<grid, THREADS, SMEM, s>>>(pcm, (long long)n, (long long)stride, (long long)total, mel, wmax);
     const int per4 = N_FRAMES * n_mels / 4;
-    dim3 cgrid((per4 + 255) / 256, batch);
+    const dim3 cgrid((per4 + 256 * CL_PER - 1) / (256 * CL_PER), batch);
     k_clamp<<<cgrid, 256, 0, s>>>(reinterpret_cast<float4 *>(mel), per4, wmax);
     count_launch(2);
     return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
