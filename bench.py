@@ -484,7 +484,7 @@ def run_ours(args):
     if fe and fe["total_ms"] > 0:
         fe_gbs = fe["bytes"] / (fe["total_ms"] * 1e-3) / 1e9
         line["frontend"] = {"gbs": fe_gbs, "frac_hbm": fe_gbs / peaks["hbm_gbs"], "ms_per_step": fe["total_ms"] / args.steps,
-                            "bound": "instruction issue (FP32 FFT), see profiles/logmel_large_v3.md"}
+                            "bound": "shared-memory traffic and latency (FP32 FFT tiles), see profiles/logmel_large_v3.md"}
     line.update(nxt)
     if e2e_ms is not None:
         line["e2e"] = {"value": B * ws * 1000.0 / e2e_ms, "unit": "windows/s",

@@ -4,8 +4,8 @@
 // power re^2 + im^2 on the 201 x 3000 grid, Slaney area-normalised mel filters, log10,
 // clamp at (window maximum - 8) and (x + 4) / 4.
 //
-// Kernel 1 (k_logmel): one block = a tile of 32 consecutive frames of one window, one frame
-// per lane.  The 5360 samples the tile touches are staged once in shared memory (coalesced;
+// k_logmel: a persistent grid; one block transforms a tile of 32 consecutive frames of one
+// window at a time, one frame per lane.  The 5360 samples the tile touches are staged once in shared memory (coalesced;
 // reflect and zero-extension applied while loading), two pad floats after every 160 samples
 // so that the 32 frames' rows start in distinct banks.  Each real 400-point frame x is
 // transformed as the complex 200-point FFT of z[m] = w[2m] x[2m] + i w[2m+1] x[2m+1] (w the
@@ -15,12 +15,13 @@
 // i.e. 8-point DFTs over n1 then 25-point DFTs (5 x 5) over n2, with no twiddles between the
 // two (8 and 25 are coprime).  The real spectrum X[k] = E[k] + W400^k O[k] (E, O the spectra
 // of the even and odd samples) and its power follow, two mirrored bins (k, 200 - k) at a
-// time; then the sparse mel projection, log10 and the tile's maximum; one atomicMax per block
+// time; then the sparse mel projection, log10 and the tile's maximum; one atomicMax per tile
 // builds the per-window maximum.  Every stage keeps lanes on frames and the warp on one
 // index of the transform, so shared-memory accesses are conflict-free and the constant
 // tables (window, gather offsets, W400^k, mel filters) are read at warp-uniform addresses.
-// Kernel 2 (k_clamp): mel = (max(mel, g - 8) + 4) / 4 in place with the window maximum g.
-// Both read/write only the PCM and the log-mel (the intermediates never reach HBM).
+// After a grid-wide barrier the same grid clamps: mel = (max(mel, g - 8) + 4) / 4 in place with
+// the window maximum g.  Only the PCM and the log-mel touch global memory (the intermediates
+// never leave shared memory).
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -50,6 +51,8 @@ constexpr int MT_STRIDE = 129;                    // log-mel tile row (odd: conf
 constexpr int MAXW = 512;                         // mel filter nonzeros (<= 2 per bin)
 constexpr size_t SMEM = (size_t)R1_FLOATS * 4 + (size_t)R2_FLOAT2 * 8;
 constexpr int A_TABLE = (SEG_FLOATS + 3) / 4 * 4;  // stage-A table above the staged samples
+constexpr int TILES = (N_FRAMES + TF - 1) / TF;    // tiles per window
+constexpr int PF = (SPAN / 4 + THREADS - 1) / THREADS;  // prefetched float4 per thread
 static_assert(A_TABLE + N2 * 24 <= R1_FLOATS, "stage-A table must fit beside the samples");
 static_assert(TF * MT_STRIDE <= 2 * R2_FLOAT2, "log-mel tile must fit the spectrum region");
 static_assert((R1_FLOATS * 4) % 16 == 0, "spectrum region alignment");
@@ -182,21 +185,30 @@ __device__ __forceinline__ void dft8_windowed(const float2 (&x)[8], const float2
 //   Y0 = y0 + t1 + t2,
 //   Y1, Y4 = y0 + c1 t1 + c2 t2 -/+ i (s1 t3 + s2 t4),
 //   Y2, Y3 = y0 + c2 t1 + c1 t2 -/+ i (s2 t3 - s1 t4),
-// c1, s1 = cos, sin (2 pi / 5) and c2, s2 = cos, sin (4 pi / 5).
-__device__ __forceinline__ void dft5(float2 &y0, float2 &y1, float2 &y2, float2 &y3, float2 &y4) {
+// c1, s1 = cos, sin (2 pi / 5) and c2, s2 = cos, sin (4 pi / 5).  Each complex value is one
+// packed (re, im) pair: complex sums and real scalings are single f32x2 instructions, and
+// -/+ i u is the swapped pair times (1, -1) or (-1, 1).
+__device__ __forceinline__ float2 p_add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 p_mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 p_fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ void dft5p(float2 &y0, float2 &y1, float2 &y2, float2 &y3, float2 &y4) {
     const float c1 = 0.30901699437494745f, c2 = -0.80901699437494734f;
     const float s1 = 0.95105651629515353f, s2 = 0.58778525229247325f;
-    const float2 t1 = make_float2(y1.x + y4.x, y1.y + y4.y), t2 = make_float2(y2.x + y3.x, y2.y + y3.y);
-    const float2 t3 = make_float2(y1.x - y4.x, y1.y - y4.y), t4 = make_float2(y2.x - y3.x, y2.y - y3.y);
-    const float2 a = make_float2(y0.x + c1 * t1.x + c2 * t2.x, y0.y + c1 * t1.y + c2 * t2.y);
-    const float2 c = make_float2(y0.x + c2 * t1.x + c1 * t2.x, y0.y + c2 * t1.y + c1 * t2.y);
-    const float2 u = make_float2(s1 * t3.x + s2 * t4.x, s1 * t3.y + s2 * t4.y);
-    const float2 v = make_float2(s2 * t3.x - s1 * t4.x, s2 * t3.y - s1 * t4.y);
-    y0 = make_float2(y0.x + t1.x + t2.x, y0.y + t1.y + t2.y);
-    y1 = make_float2(a.x + u.y, a.y - u.x);   // a - i u
-    y4 = make_float2(a.x - u.y, a.y + u.x);   // a + i u
-    y2 = make_float2(c.x + v.y, c.y - v.x);
-    y3 = make_float2(c.x - v.y, c.y + v.x);
+    const float2 C1 = make_float2(c1, c1), C2 = make_float2(c2, c2);
+    const float2 S1 = make_float2(s1, s1), S2 = make_float2(s2, s2), NS1 = make_float2(-s1, -s1);
+    const float2 M1 = make_float2(-1.0f, -1.0f), PM = make_float2(1.0f, -1.0f), MP = make_float2(-1.0f, 1.0f);
+    const float2 t1 = p_add(y1, y4), t2 = p_add(y2, y3);
+    const float2 t3 = p_fma(M1, y4, y1), t4 = p_fma(M1, y3, y2);
+    const float2 a = p_fma(C2, t2, p_fma(C1, t1, y0));
+    const float2 c = p_fma(C1, t2, p_fma(C2, t1, y0));
+    const float2 u = p_fma(S2, t4, p_mul(S1, t3));
+    const float2 v = p_fma(NS1, t4, p_mul(S2, t3));
+    y0 = p_add(y0, p_add(t1, t2));
+    const float2 us = make_float2(u.y, u.x), vs = make_float2(v.y, v.x);
+    y1 = p_fma(PM, us, a);   // a - i u
+    y4 = p_fma(MP, us, a);   // a + i u
+    y2 = p_fma(PM, vs, c);
+    y3 = p_fma(MP, vs, c);
 }
 
 // 25-point DFT in place, n = 5 a + b, k = c + 5 e: 5-point DFTs over a (for each b), the
@@ -216,7 +228,7 @@ __device__ __forceinline__ void dft25(float2 (&v)[25]) {
                              -0.12533323356430429f, -0.36812455268467792f, -0.58778525229247269f,
                              -0.77051324277578936f};
 #pragma unroll
-    for (int b = 0; b < 5; ++b) dft5(v[b], v[5 + b], v[10 + b], v[15 + b], v[20 + b]);
+    for (int b = 0; b < 5; ++b) dft5p(v[b], v[5 + b], v[10 + b], v[15 + b], v[20 + b]);
     // now v[5 c + b] = U[b][c]; multiply by W25^(b c) = (cos, -sin)(2 pi b c / 25)
 #pragma unroll
     for (int b = 1; b < 5; ++b)
@@ -227,7 +239,7 @@ __device__ __forceinline__ void dft25(float2 (&v)[25]) {
             v[5 * c + b] = make_float2(a.x * cs + a.y * sn, a.y * cs - a.x * sn);
         }
 #pragma unroll
-    for (int c = 0; c < 5; ++c) dft5(v[5 * c], v[5 * c + 1], v[5 * c + 2], v[5 * c + 3], v[5 * c + 4]);
+    for (int c = 0; c < 5; ++c) dft5p(v[5 * c], v[5 * c + 1], v[5 * c + 2], v[5 * c + 3], v[5 * c + 4]);
 }
 
 // Order-preserving map float -> uint32 (for atomicMax over signed floats).
@@ -242,21 +254,21 @@ __device__ __forceinline__ float key2f(uint32_t k) {
 // Stage A: frame = lane, n2 = warp, warp + 8, ...: the 8-point DFT over n1 of the windowed
 // z[(25 n1 + 8 n2) mod 200], stored at [k1][n2][frame].  The window pairs and gather offsets
 // of each n2 come from a small table in shared memory (one broadcast read per value).
+__device__ __forceinline__ void dft8_item(const float *__restrict__ xf, const ARow *__restrict__ r,
+                                          float2 *__restrict__ dst) {
+    float2 u[8], y[8], w[8];
+#pragma unroll
+    for (int n1 = 0; n1 < 8; ++n1) {
+        w[n1] = r->w[n1];
+        u[n1] = *reinterpret_cast<const float2 *>(xf + r->off[n1]);
+    }
+    dft8_windowed(u, w, y);
+#pragma unroll
+    for (int k1 = 0; k1 < 8; ++k1) dst[k1 * N2 * TF] = y[k1];
+}
 __device__ __forceinline__ void stage_a(const float *__restrict__ xf, const ARow *__restrict__ at,
                                         float2 *__restrict__ R2, int warp, int lane) {
-    for (int n2 = warp; n2 < N2; n2 += NWARP) {
-        const ARow *r = at + n2;
-        float2 u[8], y[8], w[8];
-#pragma unroll
-        for (int n1 = 0; n1 < 8; ++n1) {
-            w[n1] = r->w[n1];
-            u[n1] = *reinterpret_cast<const float2 *>(xf + r->off[n1]);
-        }
-        dft8_windowed(u, w, y);
-        float2 *dst = R2 + n2 * TF + lane;
-#pragma unroll
-        for (int k1 = 0; k1 < 8; ++k1) dst[k1 * N2 * TF] = y[k1];
-    }
+    for (int n2 = warp; n2 < N2; n2 += NWARP) dft8_item(xf, at + n2, R2 + n2 * TF + lane);
 }
 
 // Stage C: frame = lane, bin pairs (k, 200 - k) with k = warp + 8 i in 1 .. 100.  Z[k] sits at
@@ -268,6 +280,7 @@ __device__ __forceinline__ void stage_c(const float2 *__restrict__ R2, float *__
     const float2 *zb = R2 + ((8 - warp) & 7) * N2 * TF + lane;      // (200 - k) mod 8
     int k = warp == 0 ? NWARP : warp;
     int ka = k % 25;                                                // k mod 25
+#pragma unroll 4
     for (; k <= 100; k += NWARP) {
         const int kb = ka == 0 ? 0 : 25 - ka;                       // (200 - k) mod 25
         const float2 A = za[ka * TF];
@@ -321,125 +334,213 @@ __device__ __forceinline__ void stage_d(const float *__restrict__ P, float *__re
 // Window b starts at pcm + b * stride and holds min(n, total - b * stride) samples (a batch of
 // clips: stride = n, total = batch * n; one long clip cut into 30-s windows: stride = n =
 // 480000, total = the clip's length).
+struct Tile {
+    const float *x;   // the window's first sample
+    long long n;      // samples the window holds
+    long long s0;     // span start (160 t0 - 200)
+    int b, t0, nf;
+    bool fast;        // the span lies inside the clip and is 16-byte aligned
+};
+__device__ __forceinline__ Tile tile_of(int t, const float *pcm, long long n, long long stride, long long total) {
+    Tile T;
+    T.b = t / TILES;
+    T.t0 = (t - T.b * TILES) * TF;
+    T.nf = min(TF, N_FRAMES - T.t0);
+    T.x = pcm + (long long)T.b * stride;
+    T.n = min(n, total - (long long)T.b * stride);
+    T.s0 = (long long)HOP * T.t0 - N_FFT / 2;
+    const long long lim = T.n < N_SAMPLES ? T.n : N_SAMPLES;
+    T.fast = T.s0 >= 0 && T.s0 + SPAN <= lim && ((reinterpret_cast<uintptr_t>(T.x + T.s0) & 15) == 0);
+    return T;
+}
+
+// One persistent grid (all blocks resident: a cooperative launch) walks the tiles of every
+// window; each block prefetches its next tile's samples into registers while it finishes the
+// current one.  Every tile writes its log10 values and raises its window's maximum; after a
+// grid-wide barrier all blocks apply the clamp (max(x, g - 8) + 4) / 4 to an equal share of
+// the output.  ws holds the batch's window maxima (order-preserving keys) then the barrier's
+// arrival count, all zero at launch.
 template <int NM>
-__global__ void __launch_bounds__(THREADS, 3) k_logmel(const float *__restrict__ pcm, long long n, long long stride,
-                                                       long long total, float *__restrict__ mel,
-                                                       uint32_t *__restrict__ wmax) {
+__global__ void __launch_bounds__(THREADS, 2) k_logmel(const float *__restrict__ pcm, long long n, long long stride,
+                                                       long long total, int batch, float *__restrict__ mel,
+                                                       uint32_t *__restrict__ ws, DevCtl ctl) {
     extern __shared__ float4 smem4[];
     float *R1 = reinterpret_cast<float *>(smem4);             // staged samples, then the power [bin - 1][frame]
     float2 *R2 = reinterpret_cast<float2 *>(R1 + R1_FLOATS);  // spectra [k1][k2][frame], then the log-mel tile
     __shared__ float red[NWARP];
+    __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.y;
-    const int t0 = blockIdx.x * TF;
-    const int nf = min(TF, N_FRAMES - t0);
-    const float *x = pcm + (long long)b * stride;
-    n = min(n, total - (long long)b * stride);
+    const int tiles = TILES * batch;
+    float4 pf[PF];   // the next tile's samples (fast tiles only)
+    bool have_pf = false;
 
-    // The stage-A table (window pairs and gather offsets per n2) goes into the slack above the
-    // staged samples.
-    {
-        const int4 *src = reinterpret_cast<const int4 *>(c_arow);
-        int4 *dst = reinterpret_cast<int4 *>(R1 + A_TABLE);
-        for (int i = tid; i < (int)(sizeof(c_arow) / 16); i += THREADS) dst[i] = src[i];
-    }
-
-    // Stage samples 160 t0 - 200 ... (pad/truncate to 480000, then reflect by 200).  Tiles
-    // whose span lies inside the clip and is 16-byte aligned copy with float4 loads.
-    const long long s0 = (long long)HOP * t0 - N_FFT / 2;
-    const long long lim = n < N_SAMPLES ? n : N_SAMPLES;
-    if (s0 >= 0 && s0 + SPAN <= lim && ((reinterpret_cast<uintptr_t>(x + s0) & 15) == 0)) {
-        const float4 *src = reinterpret_cast<const float4 *>(x + s0);
-        for (int q = tid; q < SPAN / 4; q += THREADS) {
-            const float4 v = __ldg(src + q);
-            float *d = R1 + seg_pos(4 * q);   // the four samples share a row (160 % 4 == 0)
-            *reinterpret_cast<float2 *>(d) = make_float2(v.x, v.y);
-            *reinterpret_cast<float2 *>(d + 2) = make_float2(v.z, v.w);
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        // The stage-A table (window pairs and gather offsets per n2) goes into the slack above
+        // the staged samples; then the samples 160 t0 - 200 ... (pad/truncate to 480000, then
+        // reflect by 200), from the prefetch registers or straight from global memory.
+        {
+            const int4 *src = reinterpret_cast<const int4 *>(c_arow);
+            int4 *dst = reinterpret_cast<int4 *>(R1 + A_TABLE);
+            for (int i = tid; i < (int)(sizeof(c_arow) / 16); i += THREADS) dst[i] = src[i];
         }
-    } else {
-        for (int j = tid; j < SPAN; j += THREADS) {
-            long long si = s0 + j;
-            si = si < 0 ? -si : si;
-            si = si > N_SAMPLES - 1 ? 2LL * (N_SAMPLES - 1) - si : si;
-            R1[seg_pos(j)] = (si < n) ? __ldg(x + si) : 0.0f;
+        if (have_pf) {
+#pragma unroll
+            for (int u = 0; u < PF; ++u) {
+                const int q = tid + u * THREADS;
+                if (q < SPAN / 4) {
+                    float *d = R1 + seg_pos(4 * q);   // the four samples share a row (160 % 4 == 0)
+                    *reinterpret_cast<float2 *>(d) = make_float2(pf[u].x, pf[u].y);
+                    *reinterpret_cast<float2 *>(d + 2) = make_float2(pf[u].z, pf[u].w);
+                }
+            }
+        } else {
+            const Tile T = tile_of(t, pcm, n, stride, total);
+            if (T.fast) {
+                const float4 *src = reinterpret_cast<const float4 *>(T.x + T.s0);
+                for (int q = tid; q < SPAN / 4; q += THREADS) {
+                    const float4 v = __ldg(src + q);
+                    float *d = R1 + seg_pos(4 * q);
+                    *reinterpret_cast<float2 *>(d) = make_float2(v.x, v.y);
+                    *reinterpret_cast<float2 *>(d + 2) = make_float2(v.z, v.w);
+                }
+            } else {
+                for (int j = tid; j < SPAN; j += THREADS) {
+                    long long si = T.s0 + j;
+                    si = si < 0 ? -si : si;
+                    si = si > N_SAMPLES - 1 ? 2LL * (N_SAMPLES - 1) - si : si;
+                    R1[seg_pos(j)] = (si < T.n) ? __ldg(T.x + si) : 0.0f;
+                }
+            }
         }
-    }
-    __syncthreads();
+        __syncthreads();
 
-    stage_a(R1 + ROW * lane, reinterpret_cast<const ARow *>(R1 + A_TABLE), R2, warp, lane);
-    __syncthreads();
+        stage_a(R1 + ROW * lane, reinterpret_cast<const ARow *>(R1 + A_TABLE), R2, warp, lane);
+        __syncthreads();
 
-    // Stage B: frame = lane, k1 = warp: the 25-point DFT over n2, in place;
-    // [k1][k2][frame] then holds Z[(25 k1 + 176 k2) mod 200].
-    {
-        float2 *col = R2 + warp * N2 * TF + lane;
-        float2 v[25];
+        // Stage B: frame = lane, k1 = warp: the 25-point DFT over n2, in place;
+        // [k1][k2][frame] then holds Z[(25 k1 + 176 k2) mod 200].
+        {
+            float2 *col = R2 + warp * N2 * TF + lane;
+            float2 v[25];
 #pragma unroll
-        for (int i = 0; i < 25; ++i) v[i] = col[i * TF];
-        dft25(v);
+            for (int i = 0; i < 25; ++i) v[i] = col[i * TF];
+            dft25(v);
 #pragma unroll
-        for (int c = 0; c < 5; ++c)
+            for (int c = 0; c < 5; ++c)
 #pragma unroll
-            for (int e = 0; e < 5; ++e) col[(c + 5 * e) * TF] = v[5 * c + e];
-    }
-    __syncthreads();
+                for (int e = 0; e < 5; ++e) col[(c + 5 * e) * TF] = v[5 * c + e];
+        }
+        __syncthreads();
 
-    float *P = R1;
-    stage_c(R2, P, warp, lane);
-    __syncthreads();
+        // Prefetch the next tile's samples (the loads complete behind stages C and D).
+        {
+            const int tn = t + gridDim.x;
+            have_pf = false;
+            if (tn < tiles) {
+                const Tile N = tile_of(tn, pcm, n, stride, total);
+                if (N.fast) {
+                    const float4 *src = reinterpret_cast<const float4 *>(N.x + N.s0);
+#pragma unroll
+                    for (int u = 0; u < PF; ++u) {
+                        const int q = tid + u * THREADS;
+                        if (q < SPAN / 4) pf[u] = __ldg(src + q);
+                    }
+                    have_pf = true;
+                }
+            }
+        }
 
-    float lmax = -INFINITY;
-    float *Mt = reinterpret_cast<float *>(R2);
-    const bool valid = lane < nf;
+        float *P = R1;
+        stage_c(R2, P, warp, lane);
+        __syncthreads();
+
+        const int tb = t / TILES, t0 = (t - tb * TILES) * TF, nf = min(TF, N_FRAMES - t0);
+        float lmax = -INFINITY;
+        float *Mt = reinterpret_cast<float *>(R2);
+        const bool valid = lane < nf;
 #define WH_STAGE_D(w) stage_d<NM, w, 0>(P, Mt, lane, valid, lmax)
-    WH_WARP_SWITCH(WH_STAGE_D)
+        WH_WARP_SWITCH(WH_STAGE_D)
 #undef WH_STAGE_D
-    __syncthreads();
+        __syncthreads();
 
-    // Frame-major store: one row of NM per frame, lanes over m (coalesced).
-    float *out = mel + ((long long)b * N_FRAMES + t0) * NM;
-    for (int f = warp; f < nf; f += NWARP) {
+        // Frame-major store of the log10 values: one row of NM per frame, lanes over m.
+        float *out = mel + ((long long)tb * N_FRAMES + t0) * NM;
 #pragma unroll
-        for (int m0 = 0; m0 < NM; m0 += 32)
-            if (m0 + lane < NM) out[(long long)f * NM + m0 + lane] = Mt[f * MT_STRIDE + m0 + lane];
+        for (int f = warp; f < TF; f += NWARP) {
+            if (f >= nf) break;
+#pragma unroll
+            for (int m0 = 0; m0 < NM; m0 += 32)
+                if (m0 + lane < NM) out[(long long)f * NM + m0 + lane] = Mt[f * MT_STRIDE + m0 + lane];
+        }
+        lmax = warp_max(lmax);
+        if (lane == 0) red[warp] = lmax;
+        __syncthreads();   // also: this tile's shared-memory reads are done before the next staging
+        if (tid < 32) {
+            float v = tid < NWARP ? red[tid] : -INFINITY;
+            v = warp_max(v);
+            if (tid == 0) atomicMax(ws + tb, f2key(v));
+        }
     }
 
-    lmax = warp_max(lmax);
-    if (lane == 0) red[warp] = lmax;
+    // Grid-wide barrier: every tile's values and maxima are written.  Bounded: on expiry the
+    // status word records WH_ETIMEOUT and the block returns without clamping.
     __syncthreads();
-    if (tid < 32) {
-        float v = tid < NWARP ? red[tid] : -INFINITY;
-        v = warp_max(v);
-        if (tid == 0) atomicMax(wmax + b, f2key(v));
+    if (tid == 0) {
+        int ok = 1;
+        __threadfence();
+        atomicAdd(ws + batch, 1u);
+        const uint64_t t_start = globaltimer_ns();
+        for (uint32_t it = 0;; ++it) {
+            uint32_t arrived;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(arrived) : "l"(ws + batch) : "memory");
+            if (arrived >= gridDim.x) break;
+            if ((it & 63u) == 63u && globaltimer_ns() - t_start > ctl.wait_ns) {
+                set_status(ctl, WH_ETIMEOUT);
+                ok = 0;
+                break;
+            }
+        }
+        abort_flag = !ok;
+    }
+    __syncthreads();
+    if (abort_flag) return;
+
+    // Clamp, an equal share per block: mel = (max(mel, g_b - 8) + 4) / 4, g_b window b's maximum.
+    // A share is shorter than a window, so it spans at most two windows; eight float4 per
+    // thread are in flight at a time.
+    constexpr int PER_WINDOW4 = N_FRAMES * NM / 4;
+    constexpr int CU = 8;
+    const long long all4 = (long long)batch * PER_WINDOW4;
+    const long long chunk = (all4 + gridDim.x - 1) / gridDim.x;
+    const long long lo = (long long)blockIdx.x * chunk, hi = min(all4, lo + chunk);
+    if (lo >= hi) return;
+    const int b_lo = (int)(lo / PER_WINDOW4);
+    const long long split = (long long)(b_lo + 1) * PER_WINDOW4;   // first index of window b_lo + 1
+    const float floor_lo = key2f(__ldcg(ws + b_lo)) - 8.0f;
+    const float floor_hi = split < hi ? key2f(__ldcg(ws + b_lo + 1)) - 8.0f : floor_lo;
+    float4 *m4 = reinterpret_cast<float4 *>(mel);
+    for (long long base = lo + tid; base < hi; base += CU * THREADS) {
+        float4 v[CU];
+#pragma unroll
+        for (int u = 0; u < CU; ++u)
+            if (base + u * THREADS < hi) v[u] = __ldcg(m4 + base + u * THREADS);
+#pragma unroll
+        for (int u = 0; u < CU; ++u) {
+            const long long i = base + u * THREADS;
+            if (i < hi) {
+                const float fl = i < split ? floor_lo : floor_hi;
+                float4 w = v[u];
+                w.x = (fmaxf(w.x, fl) + 4.0f) * 0.25f;
+                w.y = (fmaxf(w.y, fl) + 4.0f) * 0.25f;
+                w.z = (fmaxf(w.z, fl) + 4.0f) * 0.25f;
+                w.w = (fmaxf(w.w, fl) + 4.0f) * 0.25f;
+                m4[i] = w;
+            }
+        }
     }
 }
 #undef WH_WARP_SWITCH
-
-// grid (x, window b): mel[b] = (max(mel[b], g_b - 8) + 4) / 4 in place, g_b the window
-// maximum; each thread clamps CL_PER float4 (all loads issued before the stores).
-constexpr int CL_PER = 4;
-__global__ void __launch_bounds__(256) k_clamp(float4 *__restrict__ mel, int per_window4,
-                                               const uint32_t *__restrict__ wmax) {
-    const int b = blockIdx.y;
-    const float floor = key2f(__ldg(wmax + b)) - 8.0f;
-    float4 *w = mel + (long long)b * per_window4;
-    const int base = blockIdx.x * (256 * CL_PER) + threadIdx.x;
-    float4 v[CL_PER];
-#pragma unroll
-    for (int u = 0; u < CL_PER; ++u)
-        if (base + u * 256 < per_window4) v[u] = w[base + u * 256];
-#pragma unroll
-    for (int u = 0; u < CL_PER; ++u)
-        if (base + u * 256 < per_window4) {
-            float4 t = v[u];
-            t.x = (fmaxf(t.x, floor) + 4.0f) * 0.25f;
-            t.y = (fmaxf(t.y, floor) + 4.0f) * 0.25f;
-            t.z = (fmaxf(t.z, floor) + 4.0f) * 0.25f;
-            t.w = (fmaxf(t.w, floor) + 4.0f) * 0.25f;
-            w[base + u * 256] = t;
-        }
-}
 
 // ---- host-side constant tables (built in double precision) ----------------------------
 double hz_to_mel(double f) {  // Slaney: 3 f / 200 below 1 kHz, 27 mel per factor 6.4 above
@@ -545,18 +646,31 @@ int frontend_init_tables() {
 }
 
 int frontend_launch(const float *pcm, int64_t n, int64_t stride, int64_t total, int batch, int n_mels, float *mel,
-                    uint32_t *wmax, cudaStream_t s) {
-    if (cudaMemsetAsync(wmax, 0, sizeof(uint32_t) * (size_t)batch, s) != cudaSuccess) return WH_ECUDA;
-    const dim3 grid((N_FRAMES + TF - 1) / TF, batch);
-    if (n_mels == 128)
-        k_logmel<128><<<grid, THREADS, SMEM, s>>>(pcm, (long long)n, (long long)stride, (long long)total, mel, wmax);
-    else
-        k_logmel<80><<<grid, THREADS, SMEM, s>>>(pcm, (long long)n, (long long)stride, (long long)total, mel, wmax);
-    const int per4 = N_FRAMES * n_mels / 4;
-    const dim3 cgrid((per4 + 256 * CL_PER - 1) / (256 * CL_PER), batch);
-    k_clamp<<<cgrid, 256, 0, s>>>(reinterpret_cast<float4 *>(mel), per4, wmax);
-    count_launch(2);
-    return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
+                    uint32_t *ws, const DevCtl &ctl, int num_sms, cudaStream_t s) {
+    // window maxima and the barrier's arrival count start at zero
+    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t) * ((size_t)batch + 1), s) != cudaSuccess) return WH_ECUDA;
+    const void *fn = n_mels == 128 ? reinterpret_cast<const void *>(k_logmel<128>)
+                                   : reinterpret_cast<const void *>(k_logmel<80>);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, THREADS, SMEM) != cudaSuccess || per_sm < 1)
+        return WH_ECUDA;
+    const long long tiles = (long long)TILES * batch;
+    const long long resident = (long long)per_sm * num_sms;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)(tiles < resident ? tiles : resident));
+    lc.blockDim = dim3(THREADS);
+    lc.dynamicSmemBytes = SMEM;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every block resident: the grid barrier
+    attr[0].val.cooperative = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const long long nn = n, st = stride, tot = total;
+    const cudaError_t e = n_mels == 128 ? cudaLaunchKernelEx(&lc, k_logmel<128>, pcm, nn, st, tot, batch, mel, ws, ctl)
+                                        : cudaLaunchKernelEx(&lc, k_logmel<80>, pcm, nn, st, tot, batch, mel, ws, ctl);
+    count_launch(1);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
 }
 
 }  // namespace wh

@@ -1,7 +1,7 @@
 // wh_frontend_static: the log-mel front end for callers that cannot allocate device memory.
 //
 // wh_frontend needs a small caller-provided scratch buffer (one word per window for the
-// window's maximum log-mel value).  Some callers have no way to provide one at the point
+// window's maximum log-mel value, one for the kernel's grid barrier).  Some callers have no way to provide one at the point
 // they call in: a real-time audio callback must not block on the CUDA allocator
 // (cudaMalloc can synchronise the device and take milliseconds), and a process that has
 // handed all of its device memory to another allocator up front has none left to give.
@@ -9,7 +9,7 @@
 // allocates nothing: the caller still passes the PCM input and the log-mel output.
 //
 // The array below is a file-scope device variable: every GPU that loads the library holds
-// its WH_FRONTEND_STATIC_MAX_BATCH words until the process exits.  Host code cannot use the
+// its WH_FRONTEND_STATIC_MAX_BATCH + 1 words until the process exits.  Host code cannot use the
 // name of a device variable as an address (on the host it names a host-side stand-in), so
 // the device address is looked up once per device with cudaGetSymbolAddress and passed to
 // the kernels.  All calls on a device share the one array, so calls that overlap on the GPU
@@ -23,7 +23,7 @@
 namespace wh {
 namespace {
 
-static __device__ __align__(256) uint32_t g_frontend_scratch[WH_FRONTEND_STATIC_MAX_BATCH];
+static __device__ __align__(256) uint32_t g_frontend_scratch[WH_FRONTEND_STATIC_MAX_BATCH + 1];
 
 constexpr int MAX_DEV = 64;
 uint32_t *g_scratch_ptr[MAX_DEV] = {};
@@ -62,6 +62,11 @@ extern "C" int wh_frontend_static(const float *pcm, int64_t n, int batch, int n_
     if (!mel || (n > 0 && !pcm) || (reinterpret_cast<uintptr_t>(mel) % 16) != 0) return WH_EINVAL;
     uint32_t *scratch = nullptr;
     if (int rc = scratch_for_current_device(&scratch)) return rc;
-    // frontend_launch clears the per-window maxima (cudaMemsetAsync) before its kernels run.
-    return frontend_launch(pcm, n, n, n * batch, batch, n_mels, mel, scratch, static_cast<cudaStream_t>(stream));
+    DevCtl ctl;
+    int num_sms = 0;
+    if (int rc = frontend_ctl(&ctl, &num_sms)) return rc;
+    // frontend_launch clears the per-window maxima and the barrier count (cudaMemsetAsync)
+    // before its kernel runs.
+    return frontend_launch(pcm, n, n, n * batch, batch, n_mels, mel, scratch, ctl, num_sms,
+                           static_cast<cudaStream_t>(stream));
 }

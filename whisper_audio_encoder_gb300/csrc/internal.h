@@ -43,8 +43,8 @@ int gemm_prepare(int num_sms);
 int frontend_init_tables();   // once per device (current device)
 // window b: pcm + b * stride, min(n, total - b * stride) samples
 int frontend_launch(const float *pcm, int64_t n, int64_t stride, int64_t total, int batch, int n_mels, float *mel,
-                    uint32_t *wmax,
-                    cudaStream_t s);
+                    uint32_t *ws, const DevCtl &ctl, int num_sms, cudaStream_t s);
+int frontend_ctl(DevCtl *ctl, int *num_sms);   // the current device's control block and SM count
 
 // ---- other kernels ---------------------------------------------------------------------
 int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,

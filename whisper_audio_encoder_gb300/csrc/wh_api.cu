@@ -185,6 +185,14 @@ GemmDesc gemm(const void *a, int lda, int M, int K, const void *b, int ldb, int 
 
 void count_launch(int n) { g_launches += n; }
 
+int frontend_ctl(DevCtl *ctl, int *num_sms) {
+    DevState *st;
+    if (int rc = ensure_device(&st)) return rc;
+    *ctl = ctl_of(st);
+    *num_sms = st->num_sms;
+    return WH_OK;
+}
+
 int device_setup() {
     DevState *st;
     return ensure_device(&st);
@@ -238,7 +246,8 @@ int wh_shutdown(void) {
     return WH_OK;
 }
 
-size_t wh_frontend_workspace(int batch) { return batch <= 0 ? 0 : up256(sizeof(uint32_t) * (size_t)batch); }
+// one word per window (its maximum) and the front-end grid's barrier count
+size_t wh_frontend_workspace(int batch) { return batch <= 0 ? 0 : up256(sizeof(uint32_t) * ((size_t)batch + 1)); }
 
 int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel, void *workspace, size_t ws_bytes,
                 void *stream) {
@@ -251,7 +260,8 @@ int wh_frontend(const float *pcm, int64_t n, int batch, int n_mels, float *mel, 
     if (int rc = ensure_device(&st)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     trace_begin(TR_FRONTEND, s);
-    const int rc = frontend_launch(pcm, n, n, n * batch, batch, n_mels, mel, static_cast<uint32_t *>(workspace), s);
+    const int rc = frontend_launch(pcm, n, n, n * batch, batch, n_mels, mel, static_cast<uint32_t *>(workspace),
+                                   ctl_of(st), st->num_sms, s);
     const double n_read = (double)(n < 480000 ? n : 480000);
     trace_end(TR_FRONTEND, s, 0.0, batch * (n_read * 4.0 + 3000.0 * n_mels * 4.0));
     return rc;
@@ -276,7 +286,7 @@ int wh_frontend_long(const float *pcm, int64_t n_total, int n_mels, float *mel, 
     const int64_t win = (int64_t)N_FRAMES * 160;  // 480000 samples, 30 s
     trace_begin(TR_FRONTEND, s);
     const int rc = frontend_launch(pcm, win, win, n_total, (int)windows, n_mels, mel,
-                                   static_cast<uint32_t *>(workspace), s);
+                                   static_cast<uint32_t *>(workspace), ctl_of(st), st->num_sms, s);
     trace_end(TR_FRONTEND, s, 0.0, (double)n_total * 4.0 + (double)windows * N_FRAMES * n_mels * 4.0);
     return rc;
 }
