@@ -85,7 +85,11 @@ typedef struct {
  *   mel   device float32 [batch][3000][n_mels]: per window 3000 rows of n_mels values, each
  *         frame contiguous (the layout "whisper 0.9.0 API" gives for wh_encode's input).
  *   workspace  device scratch of at least wh_frontend_workspace(batch) bytes, 16-byte aligned
- *         (the per-window maxima); contents need not be initialised.
+ *         (the per-window maxima and the kernel's grid-barrier count: batch + 1 words);
+ *         contents need not be initialised.
+ * The work is one cooperative launch (every block resident at once) with a grid-wide barrier
+ * between the log10 values and the clamp; the barrier's wait is bounded (1 s): if it runs
+ * out, wh_status() reports WH_ETIMEOUT and the output is left unclamped.
  * Errors: WH_EINVAL (null pointer with batch > 0, n < 0, batch < 0 or > 65535, n_mels not
  *         80/128), WH_ENOSPC (workspace too small), WH_ECUDA.  batch == 0 is a no-op.
  * ------------------------------------------------------------------------------------ */
@@ -134,7 +138,7 @@ int wh_resample(const float *x, int64_t n_in, int batch, int rate_in, float *y, 
  * Some callers cannot hand the library a scratch buffer at the point they call in: a
  * real-time audio callback must not block on the CUDA allocator, and a process that gave
  * all of its device memory to another allocator up front has none left.  This variant keeps
- * the per-window maxima in a fixed array inside the library (WH_FRONTEND_STATIC_MAX_BATCH
+ * the per-window maxima in a fixed array inside the library (WH_FRONTEND_STATIC_MAX_BATCH + 1
  * words, held on every GPU that loads the library until the process exits) and allocates
  * nothing; pcm and mel are as for wh_frontend.
  *   - batch > WH_FRONTEND_STATIC_MAX_BATCH returns WH_ENOSPC (nothing is launched).

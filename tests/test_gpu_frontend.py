@@ -67,3 +67,19 @@ def test_batch_position_does_not_change_the_result():
     pcm = np.stack([synth.waveform(cfg, 1), x, synth.waveform(cfg, 2), x])
     mel = wh.wh_frontend(torch.from_numpy(pcm).cuda(), 80).cpu().numpy()
     assert np.array_equal(mel[1], mel[3])
+
+
+def test_grid_shape_does_not_change_the_result():
+    # Alone, the window's 94 tiles each get their own block.  In a batch of 40 windows (3760
+    # tiles) every block of the resident grid walks many tiles of several windows and loads
+    # each next tile's samples ahead.  Either way each tile is computed the same: bitwise equal.
+    cfg = configs.CONFIGS[2]
+    x = synth.waveform(cfg, 5)
+    alone = wh.wh_frontend(torch.from_numpy(x[None, :].copy()).cuda(), 80).cpu().numpy()[0]
+    rng = np.random.default_rng(40)
+    pcm = (0.05 * rng.standard_normal((40, 480_000))).astype(np.float32)
+    pcm[17] = x
+    many = wh.wh_frontend(torch.from_numpy(pcm).cuda(), 80).cpu().numpy()
+    assert wh.wh_status() == wh.WH_OK
+    assert np.array_equal(alone, many[17])
+    assert maxabs(many[39], R.log_mel(pcm[39], 80)) <= LOGMEL_ATOL
