@@ -75,8 +75,10 @@ def _peaks():
         with open(path) as fh:
             d = json.load(fh)
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
 
 
 def _workload(cfg, n_gpus):
@@ -101,6 +103,7 @@ def _oracle_sample(cfg, reps=1):
     pcm = synth.waveform(cfg, 0)
     w = synth.weights(cfg, layers=[0])
     best = None
+    parts = None
     for _ in range(reps):
         t0 = time.perf_counter()
         mel = R.log_mel(pcm, cfg.n_mels)
@@ -112,11 +115,14 @@ def _oracle_sample(cfg, reps=1):
         R.layer_norm(x, np.asarray(w["lnf_g"], np.float64), np.asarray(w["lnf_b"], np.float64))
         t4 = time.perf_counter()
         per_window = (t1 - t0) + (t2 - t1) + cfg.n_layer * (t3 - t2) + (t4 - t3)
-        best = per_window if best is None else min(best, per_window)
+        if best is None or per_window < best:
+            best = per_window
+            parts = {"frontend_s": t1 - t0, "encoder_s": per_window - (t1 - t0)}
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     sample = (f"window 0 of {cfg.name}: oracle front end, conv stem, 1 of {cfg.n_layer} blocks and final "
               f"LayerNorm (float64 NumPy, BLAS threads = host cores); window time = fe + stem + "
               f"{cfg.n_layer} x block + norm, best of {reps}")
+    _oracle_sample.parts = parts   # the front end (the fp64 DFT) and the encoder, s per window
     return 1.0 / best, cores, sample
 
 
@@ -483,6 +489,20 @@ def run_ours(args):
     fe = stats.get("frontend")
     if fe and fe["total_ms"] > 0:
         fe_gbs = fe["bytes"] / (fe["total_ms"] * 1e-3) / 1e9
+        # FP32 side of the front end: algorithmic flops per frame = 2.5 N log2 N for the real
+        # 400-point FFT, 3 per bin for the power (201 bins), 2 per mel-filter weight (391 of
+        # them for 80 mels, 394 for 128) and 1 per log10; the peak is the SMs x 128 FP32 lanes
+        # x 2 flops (FMA) x the maximum SM clock.
+        import math
+        taps = 391 if cfg.n_mels == 80 else 394
+        fe_flops = B * 3000 * (2.5 * 400 * math.log2(400) + 3 * 201 + 2 * taps + cfg.n_mels)
+        fe_tf = fe_flops * args.steps / (fe["total_ms"] * 1e-3) / 1e12
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        fp32_peak = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        line["frontend_fp32"] = {"tflops": fe_tf, "peak": fp32_peak, "frac": fe_tf / fp32_peak,
+                                 "flops_per_step": fe_flops,
+                                 "peak_source": f"nominal: {sms} SMs x 128 FP32 lanes x 2 flops x "
+                                                f"{peaks['sm_max_mhz']:.0f} MHz"}
         line["frontend"] = {"gbs": fe_gbs, "frac_hbm": fe_gbs / peaks["hbm_gbs"], "ms_per_step": fe["total_ms"] / args.steps,
                             "bound": "shared-memory traffic and latency (FP32 FFT tiles), see profiles/logmel_large_v3.md"}
     line.update(nxt)
@@ -491,7 +511,8 @@ def run_ours(args):
                        "h2d_bytes_per_step": int(pcm_h.numel() * 4), "d2h_bytes_per_step": int(out_h.numel() * 4)}
     if ws == 1 and not args.no_cpu_baseline:
         v, cores, sample = _oracle_sample(cfg)
-        line["cpu_baseline"] = {"value": v, "unit": "windows/s", "cores": cores, "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = {"value": v, "unit": "windows/s", "cores": cores, "kind": "oracle", "sample": sample,
+                                "s_per_window": _oracle_sample.parts}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
