@@ -65,10 +65,7 @@ struct ARow {
 };
 __constant__ ARow c_arow[N2];
 __constant__ float2 c_tw[101];          // W400^k = (cos, -sin)(2 pi k / 400), k = 0 .. 100
-__constant__ int c_mel_start[2][128];   // first nonzero bin of filter m
-__constant__ int c_mel_len[2][128];     // number of nonzero bins
-__constant__ int c_mel_off[2][128];     // offset of its weights in c_mel_w
-__constant__ float c_mel_w[2][MAXW];    // filter weights / 4 (the power is kept x 4)
+__constant__ float c_mel_w[2][MAXW];    // filter weights / 4 (the power is kept x 4), filter by filter
 
 // ---- compile-time shape of the transform and of the mel filters ------------------------
 // Staged offset (within a frame row) of sample 2m for z index m = (25 n1 + 8 n2) mod 200.
@@ -612,31 +609,23 @@ int frontend_init_tables() {
         if (build_rc == WH_OK) build_rc = build_mel(128, mt[1]);
     });
     if (build_rc != WH_OK) return build_rc;
-    int start[2][128], len[2][128], off[2][128];
     float w[2][MAXW];
     for (int t = 0; t < 2; ++t) {
-        for (int m = 0; m < 128; ++m) {
-            start[t][m] = mt[t].start[m];
-            len[t][m] = mt[t].len[m];
-            off[t][m] = mt[t].off[m];
-            // the kernel stores the power of bins 1 .. 199 only and unrolls each filter over the
-            // bins its compile-time shape names: both must hold for the table built here
-            const int nm = t ? 128 : 80;
-            if (m < nm) {
-                if (start[t][m] < 1 || start[t][m] + len[t][m] - 1 > N_BINS - 2) return WH_EINVAL;
-                const int cs = t ? Mel<128>::shape.start[m] : Mel<80>::shape.start[m];
-                const int cl = t ? Mel<128>::shape.len[m] : Mel<80>::shape.len[m];
-                const int co = t ? Mel<128>::shape.off[m] : Mel<80>::shape.off[m];
-                if (cs != start[t][m] || cl != len[t][m] || co != off[t][m]) return WH_EINVAL;
-            }
+        // The kernel stores the power of bins 1 .. 199 only and unrolls each filter over the
+        // bins its compile-time shape names: both must hold for the table built here.
+        const int nm = t ? 128 : 80;
+        for (int m = 0; m < nm; ++m) {
+            const int start = mt[t].start[m], len = mt[t].len[m], off = mt[t].off[m];
+            if (start < 1 || start + len - 1 > N_BINS - 2) return WH_EINVAL;
+            const int cs = t ? Mel<128>::shape.start[m] : Mel<80>::shape.start[m];
+            const int cl = t ? Mel<128>::shape.len[m] : Mel<80>::shape.len[m];
+            const int co = t ? Mel<128>::shape.off[m] : Mel<80>::shape.off[m];
+            if (cs != start || cl != len || co != off) return WH_EINVAL;
         }
         for (int i = 0; i < MAXW; ++i) w[t][i] = 0.25f * mt[t].w[i];
     }
     if (cudaMemcpyToSymbol(c_arow, arow, sizeof(arow)) != cudaSuccess ||
         cudaMemcpyToSymbol(c_tw, tw, sizeof(tw)) != cudaSuccess ||
-        cudaMemcpyToSymbol(c_mel_start, start, sizeof(start)) != cudaSuccess ||
-        cudaMemcpyToSymbol(c_mel_len, len, sizeof(len)) != cudaSuccess ||
-        cudaMemcpyToSymbol(c_mel_off, off, sizeof(off)) != cudaSuccess ||
         cudaMemcpyToSymbol(c_mel_w, w, sizeof(w)) != cudaSuccess)
         return WH_ECUDA;
     if (cudaFuncSetAttribute(k_logmel<80>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) != cudaSuccess ||
