@@ -276,8 +276,10 @@ int wh_attention(const wh_bf16 *qkv, int batch, int n_ctx, int n_head, wh_bf16 *
  *         k + b * seq_stride + t * row_stride + 64 h (likewise v).  wh_prepare_cross's rows
  *         give row_stride = 2 d_model, seq_stride = n_ctx * 2 d_model, v = k + d_model; a
  *         self-attention cache [batch][max][d_model] gives row_stride = d_model.
- *   n_keys  device int32 [batch] (each clamped to 0 .. max_keys), or NULL: max_keys for all.
- *         A sequence with no keys gets zeros.
+ *   n_keys  device int32 [batch], or NULL: max_keys for all.  A sequence with no keys gets
+ *         zeros.  The counts live in device memory, so they are checked on the device: a
+ *         count below 0 or above max_keys is clamped to that range (nothing outside it is
+ *         read) and recorded as WH_EBOUNDS, which wh_status() then returns.
  *   out   device bf16 [batch][64 n_head]
  *   workspace  >= wh_decode_attention_workspace(batch, n_head, max_keys) bytes, 256-byte
  *         aligned, contents need not be initialised; not shared by concurrent calls.

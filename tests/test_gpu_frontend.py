@@ -83,3 +83,32 @@ def test_grid_shape_does_not_change_the_result():
     assert wh.wh_status() == wh.WH_OK
     assert np.array_equal(alone, many[17])
     assert maxabs(many[39], R.log_mel(pcm[39], 80)) <= LOGMEL_ATOL
+
+
+@pytest.mark.parametrize("n_mels", [80, 128])
+def test_batch_larger_than_the_resident_grid(n_mels):
+    # 700 windows: more than the resident grid (about two blocks per SM), so each block's
+    # share of the clamp pass covers several whole windows.  Loud and quiet windows alternate
+    # (maxima 6 apart in log10), and each is mostly silence, so the clamp at its own
+    # maximum - 8 binds; a floor taken from a neighbouring window would show.  Every window
+    # must equal, bit for bit, the same window transformed alone.
+    rng = np.random.default_rng(700 + n_mels)
+    loud = (0.3 * rng.standard_normal(1000)).astype(np.float32)
+    quiet = (1e-3 * loud).astype(np.float32)
+    batch = 700
+    pcm = np.empty((batch, 1000), np.float32)
+    pcm[0::2] = loud
+    pcm[1::2] = quiet
+    pcm[5] = 0.0                                   # one silent window as well
+    mel = wh.wh_frontend(torch.from_numpy(pcm).cuda(), n_mels)
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    alone = {key: wh.wh_frontend(torch.from_numpy(x[None, :].copy()).cuda(), n_mels)[0]
+             for key, x in (("loud", loud), ("quiet", quiet))}
+    for key, x in (("loud", loud), ("quiet", quiet)):
+        assert maxabs(alone[key].cpu().numpy(), R.log_mel(x, n_mels)) <= LOGMEL_ATOL
+    for b in range(batch):
+        if b == 5:
+            assert bool(torch.all(mel[b] == -1.5)), "silent window"
+        else:
+            assert torch.equal(mel[b], alone["loud" if b % 2 == 0 else "quiet"]), f"window {b}"

@@ -209,6 +209,30 @@ def test_decode_attention_ragged_self_cache():
             _check_attend(out[b], q[b], k[b, :n], v[b, :n], n_head, f"sequence {b} ({n} keys)")
 
 
+def test_decode_attention_key_counts_out_of_range_report_ebounds():
+    """Per-sequence key counts live in device memory, so the kernel checks them: a count
+    above max_keys or below 0 is clamped (no row past the cache is read) and WH_EBOUNDS is
+    recorded; the result equals the call with the clamped counts, and the status word is
+    clear again afterwards."""
+    n_head, cap = 4, 200
+    D = 64 * n_head
+    rng = np.random.default_rng(33)
+    dev = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
+    q = dev(bf16_round_np(rng.standard_normal((3, D))))
+    k = dev(bf16_round_np(rng.standard_normal((3, cap, D))))
+    v = dev(bf16_round_np(rng.standard_normal((3, cap, D))))
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    bad = torch.tensor([cap + 1000, -7, 50], dtype=torch.int32, device="cuda")
+    out = wh.wh_decode_attention(q, k, v, D, cap * D, cap, n_head, n_keys=bad).clone()
+    assert wh.wh_status() == wh.WH_EBOUNDS
+    assert wh.wh_status() == wh.WH_OK                   # read and cleared
+    ok = torch.tensor([cap, 0, 50], dtype=torch.int32, device="cuda")
+    ref = wh.wh_decode_attention(q, k, v, D, cap * D, cap, n_head, n_keys=ok)
+    assert wh.wh_status() == wh.WH_OK
+    assert torch.equal(out, ref)
+
+
 def test_decode_attention_repeated_calls_reuse_the_workspace():
     """The merge tickets are reset by each call: the same workspace gives the same result."""
     rng = np.random.default_rng(32)

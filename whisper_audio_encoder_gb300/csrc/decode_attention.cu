@@ -23,24 +23,11 @@ namespace wh {
 
 namespace {
 
-#ifndef WH_DA_HEAD_MAJOR
-#define WH_DA_HEAD_MAJOR 1
-#endif
-#ifndef WH_DA_BLOCKS_PER_SM
-#define WH_DA_BLOCKS_PER_SM 2
-#endif
-#ifndef WH_DA_UNROLL
-#define WH_DA_UNROLL 2
-#endif
 // Grid order: with the head fastest, the blocks that run together read the same key rows
 // (all heads of a row are contiguous), so DRAM pages and L2 lines are shared.
-constexpr bool HEAD_MAJOR = WH_DA_HEAD_MAJOR != 0;
-constexpr int BLOCKS_PER_SM = WH_DA_BLOCKS_PER_SM;   // target blocks per SM over the grid
-constexpr int UNROLL = WH_DA_UNROLL;                 // key slots in flight per lane group
-#ifndef WH_DA_THREADS
-#define WH_DA_THREADS 256
-#endif
-constexpr int DA_THREADS = WH_DA_THREADS;
+constexpr int BLOCKS_PER_SM = 2;   // target blocks per SM over the grid
+constexpr int UNROLL = 2;          // key slots in flight per lane group
+constexpr int DA_THREADS = 256;
 constexpr int DA_WARPS = DA_THREADS / 32;
 constexpr int KEYS_PER_ITER = DA_WARPS * 8;   // 32 keys per block iteration
 constexpr int PART = 66;                      // floats per partial: m, l, o[64]
@@ -51,6 +38,7 @@ struct DecAttnArgs {
     long long row_stride, seq_stride;   // elements
     const int *n_keys;                  // device [batch] or null
     int max_keys, n_head, splits, chunk;
+    int *status;                        // per-device status word (WH_EBOUNDS)
     __nv_bfloat16 *out;
     float *part;                        // [batch * n_head * splits][PART]
     int *ticket;                        // [batch * n_head], zero on entry, zero on exit
@@ -76,10 +64,15 @@ __device__ __forceinline__ void merge_into(float &m, float &l, float *o, float m
 }
 
 __global__ void __launch_bounds__(DA_THREADS) k_decode_attention(const DecAttnArgs p) {
-    const int s = HEAD_MAJOR ? blockIdx.y : blockIdx.x, h = HEAD_MAJOR ? blockIdx.x : blockIdx.y, b = blockIdx.z;
+    const int s = blockIdx.y, h = blockIdx.x, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane >> 2, sub = lane & 3;   // key slot in the warp, 16-dim quarter
-    const int nk = p.n_keys ? min(max(p.n_keys[b], 0), p.max_keys) : p.max_keys;
+    int nk = p.max_keys;
+    if (p.n_keys) {   // a count outside 0 .. max_keys is clamped and reported as WH_EBOUNDS
+        const int want = p.n_keys[b];
+        nk = min(max(want, 0), p.max_keys);
+        if (want != nk && s == 0 && h == 0 && threadIdx.x == 0) atomicCAS(p.status, 0, WH_EBOUNDS);
+    }
     const int k0 = s * p.chunk, k1 = min(nk, k0 + p.chunk);
 
     // q quarter, scaled by log2(e) / 8
@@ -216,7 +209,7 @@ size_t decode_attention_workspace(int batch, int n_head, int max_keys) {
 
 int decode_attention_launch(const void *q, const void *k, const void *v, long long row_stride, long long seq_stride,
                             const int *n_keys, int max_keys, int batch, int n_head, void *out, void *workspace,
-                            int num_sms, cudaStream_t s) {
+                            const DevCtl &ctl, int num_sms, cudaStream_t s) {
     if (batch <= 0) return WH_OK;
     const long long bh = (long long)batch * n_head;
     // about BLOCKS_PER_SM blocks per SM in total, at least 64 keys per block, chunks a
@@ -241,12 +234,13 @@ int decode_attention_launch(const void *q, const void *k, const void *v, long lo
     a.n_head = n_head;
     a.splits = (int)splits;
     a.chunk = chunk;
+    a.status = ctl.status;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.part = static_cast<float *>(workspace);
     a.ticket = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
                                        ((bh * max_splits * PART * sizeof(float) + 255) & ~(size_t)255));
     if (splits > 1 && cudaMemsetAsync(a.ticket, 0, bh * sizeof(int), s) != cudaSuccess) return WH_ECUDA;
-    const dim3 grid = HEAD_MAJOR ? dim3(n_head, (unsigned)splits, batch) : dim3((unsigned)splits, n_head, batch);
+    const dim3 grid(n_head, (unsigned)splits, batch);
     k_decode_attention<<<grid, DA_THREADS, 0, s>>>(a);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;

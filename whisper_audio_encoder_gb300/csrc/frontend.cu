@@ -504,18 +504,19 @@ __global__ void __launch_bounds__(THREADS, 2) k_logmel(const float *__restrict__
     if (abort_flag) return;
 
     // Clamp, an equal share per block: mel = (max(mel, g_b - 8) + 4) / 4, g_b window b's maximum.
-    // A share is shorter than a window, so it spans at most two windows; eight float4 per
-    // thread are in flight at a time.
+    // A share may cover any number of windows (it is longer than a window once the batch has
+    // more windows than the grid has blocks).  A thread's indices only grow, so each thread
+    // follows the window its current index lies in and reloads the floor when it crosses
+    // into the next one; eight float4 per thread are in flight at a time.
     constexpr int PER_WINDOW4 = N_FRAMES * NM / 4;
     constexpr int CU = 8;
     const long long all4 = (long long)batch * PER_WINDOW4;
     const long long chunk = (all4 + gridDim.x - 1) / gridDim.x;
     const long long lo = (long long)blockIdx.x * chunk, hi = min(all4, lo + chunk);
     if (lo >= hi) return;
-    const int b_lo = (int)(lo / PER_WINDOW4);
-    const long long split = (long long)(b_lo + 1) * PER_WINDOW4;   // first index of window b_lo + 1
-    const float floor_lo = key2f(__ldcg(ws + b_lo)) - 8.0f;
-    const float floor_hi = split < hi ? key2f(__ldcg(ws + b_lo + 1)) - 8.0f : floor_lo;
+    int b_cur = (int)((lo + tid) / PER_WINDOW4);
+    long long next = (long long)(b_cur + 1) * PER_WINDOW4;   // first index of window b_cur + 1
+    float fl = key2f(__ldcg(ws + min(b_cur, batch - 1))) - 8.0f;
     float4 *m4 = reinterpret_cast<float4 *>(mel);
     for (long long base = lo + tid; base < hi; base += CU * THREADS) {
         float4 v[CU];
@@ -526,7 +527,11 @@ __global__ void __launch_bounds__(THREADS, 2) k_logmel(const float *__restrict__
         for (int u = 0; u < CU; ++u) {
             const long long i = base + u * THREADS;
             if (i < hi) {
-                const float fl = i < split ? floor_lo : floor_hi;
+                if (i >= next) {   // i < all4, so the window index stays below batch
+                    b_cur = (int)(i / PER_WINDOW4);
+                    next = (long long)(b_cur + 1) * PER_WINDOW4;
+                    fl = key2f(__ldcg(ws + b_cur)) - 8.0f;
+                }
                 float4 w = v[u];
                 w.x = (fmaxf(w.x, fl) + 4.0f) * 0.25f;
                 w.y = (fmaxf(w.y, fl) + 4.0f) * 0.25f;

@@ -64,7 +64,7 @@ void resample_forget();   // drops the per-rate filter normalisers (wh_shutdown)
 size_t decode_attention_workspace(int batch, int n_head, int max_keys);
 int decode_attention_launch(const void *q, const void *k, const void *v, long long row_stride, long long seq_stride,
                             const int *n_keys, int max_keys, int batch, int n_head, void *out, void *workspace,
-                            int num_sms, cudaStream_t s);
+                            const DevCtl &ctl, int num_sms, cudaStream_t s);
 // conv1's im2col matrix over the first n_frames (<= 3000) frames of each window's log-mel
 int stem_im2col_launch(const float *mel, int batch, int n_mels, int n_frames, void *a1, cudaStream_t s);
 // y (bf16) = x (float32), n a multiple of 4, both 16-byte aligned

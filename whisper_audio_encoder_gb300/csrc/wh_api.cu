@@ -461,7 +461,7 @@ int wh_decode_attention(const wh_bf16 *q, const wh_bf16 *k, const wh_bf16 *v, in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     trace_begin(TR_DEC_ATTN, s);
     const int rc = decode_attention_launch(q, k, v, row_stride, seq_stride, n_keys, max_keys, batch, n_head, out,
-                                           workspace, st->num_sms, s);
+                                           workspace, ctl_of(st), st->num_sms, s);
     trace_end(TR_DEC_ATTN, s, 4.0 * batch * (double)max_keys * 64.0 * n_head,
               (double)batch * n_head * max_keys * 256.0);
     return rc;
