@@ -39,6 +39,9 @@ Readings where the pages are silent (each is a decision, recorded with the code)
   r21 the windowed-sinc resampler is resample_poly's default design (Kaiser beta 5, 10 M
       taps on each side, unit DC gain).
   r22 long clips are cut into consecutive, non-overlapping 30-s windows, the last padded.
+  r23 a decode step writes the token's own key and value at row pos of the self-attention
+      cache first and then attends over rows 0..pos (the cache "holds what came before it";
+      the one query at the end attends to itself too, as every causal row does).
 
 Pinned by tests/test_oracle_*.py against closed forms, invariants, library routines
 (numpy.fft, torch.stft, torch.nn.functional) and brute force.  The full encoder has no
@@ -339,3 +342,64 @@ def resample_to_16k(x: np.ndarray, rate_in: int) -> np.ndarray:
         ok = (i >= 0) & (i < n) & (tap <= 2 * half)
         y[ok] += h[tap[ok]] * x[i[ok]]
     return y
+
+
+# ========================================================================================
+# One decoder step  [API] model.nu (decoder weights and state, wh_decode_step, wk_addv_row,
+# setrow, wh_argmax); [CKE] "The Full Stitched Circuit" (decoder block: causal self-attention,
+# cross-attention into the memory, feed-forward, each with its own LayerNorm and residual;
+# final norm and tied output projection), "The Decoder: Write One Token At A Time" and
+# "Decoding Token By Token" (the self-attention cache grows by one row per step)
+# ========================================================================================
+def decoder_embed(tok: int, pos: int, w: dict) -> np.ndarray:
+    """The token's row of the embedding plus row `pos` of the decoder's stored positions
+    ([API] wk_addv_row: x += embed_positions[pos])."""
+    return _f64(w["tok_embd"])[tok] + _f64(w["dec_pos"])[pos]
+
+
+def decoder_self_attention(h: np.ndarray, lw: dict, kcache: np.ndarray, vcache: np.ndarray, pos: int,
+                           n_head: int) -> np.ndarray:
+    """Self-attention of the token at position `pos` (reading r23).  Its own key and value
+    (k has no bias, like the encoder's) are written into row `pos` of the layer's caches
+    ([API] setrow), then its query attends over rows 0..pos -- what came before it plus
+    itself.  One query at the end needs no mask ([API] wh_decode_step); rows past `pos` are
+    never read.  kcache / vcache [n_text_ctx][d] are modified in place."""
+    q = h @ _f64(lw["wq"]).T + _f64(lw["bq"])
+    kcache[pos] = h @ _f64(lw["wk"]).T
+    vcache[pos] = h @ _f64(lw["wv"]).T + _f64(lw["bv"])
+    return attend_one(q, kcache[: pos + 1], vcache[: pos + 1], n_head)
+
+
+def decoder_block_step(x: np.ndarray, lw: dict, kcache, vcache, pos: int, xk, xv, n_head: int) -> np.ndarray:
+    """One decoder block for one token ([CKE] "The Full Stitched Circuit"):
+    x += out(self-attn(LN1 x)); x += x_out(cross-attn(LNx x) over the memory's cached K/V);
+    x += fc2(GELU(fc1(LN2 x))).  The cross query has a bias, its keys none ([API] model.nu)."""
+    h = layer_norm(x, _f64(lw["ln1_g"]), _f64(lw["ln1_b"]))
+    a = decoder_self_attention(h, lw, kcache, vcache, pos, n_head)
+    x = x + a @ _f64(lw["wo"]).T + _f64(lw["bo"])
+    h = layer_norm(x, _f64(lw["lnx_g"]), _f64(lw["lnx_b"]))
+    q = h @ _f64(lw["xwq"]).T + _f64(lw["xbq"])
+    a = attend_one(q, xk, xv, n_head)
+    x = x + a @ _f64(lw["xwo"]).T + _f64(lw["xbo"])
+    h = layer_norm(x, _f64(lw["ln2_g"]), _f64(lw["ln2_b"]))
+    return x + gelu(h @ _f64(lw["w1"]).T + _f64(lw["b1"])) @ _f64(lw["w2"]).T + _f64(lw["b2"])
+
+
+def decode_step(tok: int, pos: int, w: dict, kcache: list, vcache: list, xk: list, xv: list,
+                n_head: int) -> np.ndarray:
+    """[API] wh_decode_step for one sequence: token `tok` at position `pos`, with positions
+    0..pos-1 already in the self-attention caches.  Runs every decoder block (appending this
+    token's keys and values to kcache[l] / vcache[l], each [n_text_ctx][d], in place), the
+    final LayerNorm and the output projection through the token embedding (Whisper ties
+    them).  xk[l] / xv[l] [n_ctx][d] are decoder layer l's cross-attention keys and values
+    (cross_kv of the encoder memory).  Returns the logits, float64 [n_vocab]."""
+    x = decoder_embed(tok, pos, w)
+    for l, lw in enumerate(w["layers"]):
+        x = decoder_block_step(x, lw, kcache[l], vcache[l], pos, xk[l], xv[l], n_head)
+    x = layer_norm(x, _f64(w["lnf_g"]), _f64(w["lnf_b"]))
+    return _f64(w["tok_embd"]) @ x
+
+
+def greedy_token(logits: np.ndarray) -> int:
+    """[API] wh_argmax: the index of the largest logit (the first one on a tie)."""
+    return int(np.argmax(logits))

@@ -14,6 +14,7 @@ N_SAMPLES = 480_000      # 30 s at 16 kHz
 N_FRAMES = 3000          # STFT frames per window (hop 160)
 N_CTX = 1500             # encoder positions after the stride-2 conv
 SAMPLE_RATE = 16_000
+N_TEXT_CTX = 448         # decoder positions (the self-attention cache capacity)
 
 
 @dataclass(frozen=True)
@@ -33,6 +34,12 @@ class EncoderConfig:
     @property
     def head_dim(self) -> int:
         return self.d_model // self.n_head
+
+    @property
+    def n_vocab(self) -> int:
+        """Decoder vocabulary: the multilingual tokenizer's 51865 ids; large-v3 has one more
+        (an extra language token).  The pages read it from the checkpoint's header."""
+        return 51866 if self.n_mels == 128 else 51865
 
     def flops_per_window(self) -> dict:
         """Algorithmic flops of one window, counted from the definition of each step

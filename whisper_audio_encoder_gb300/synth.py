@@ -11,7 +11,7 @@ and the oracle see exactly the same weight values.
 """
 import numpy as np
 
-from .configs import N_SAMPLES, N_CTX, SAMPLE_RATE, EncoderConfig
+from .configs import N_SAMPLES, N_CTX, N_TEXT_CTX, SAMPLE_RATE, EncoderConfig
 
 
 # ----------------------------------------------------------------------------------------
@@ -184,3 +184,67 @@ def random_weights(n_mels, d_model, n_layer, d_ff, seed, ln_random=False) -> dic
         w["lnf_g"] = (1.0 + 0.2 * rng.standard_normal(d_model)).astype(np.float32)
         w["lnf_b"] = (0.1 * rng.standard_normal(d_model)).astype(np.float32)
     return w
+
+
+# ----------------------------------------------------------------------------------------
+# decoder (one decode step): weights, cross-attention keys/values, self-attention caches
+# ----------------------------------------------------------------------------------------
+_DEC_TENSORS = ["ln1_g", "ln1_b", "wq", "bq", "wk", "wv", "bv", "wo", "bo", "lnx_g", "lnx_b", "xwq", "xbq",
+                "xwo", "xbo", "ln2_g", "ln2_b", "w1", "b1", "w2", "b2"]
+
+
+def decoder_layer_weights(cfg: EncoderConfig, layer: int, ln_random: bool = False) -> dict:
+    """Decoder block `layer` (seed sequence (7 + c, 2000 + layer, t)): self-attention q/k/v/out
+    (no k bias), the cross-attention query and output projections (its k/v projections are
+    cross_weights), fc1/fc2, and three LayerNorms (ln1, lnx before the cross-attention,
+    ln2).  Matrices N(0, 0.02) rounded to bf16, biases N(0, 0.01); LayerNorm gamma as the
+    encoder's, beta 0 -- or, with ln_random, gamma 1 + N(0, 0.2) and beta N(0, 0.1) so that a
+    swapped or dropped norm parameter shows in a comparison."""
+    d, f = cfg.d_model, cfg.d_ff
+    g = lambda name: _rng(cfg, 2000 + layer, _DEC_TENSORS.index(name))
+    w = {}
+    for name in ("wq", "wk", "wv", "wo", "xwq", "xwo"):
+        w[name] = bf16_round(_normal(g(name), (d, d), 0.02))
+    w["w1"] = bf16_round(_normal(g("w1"), (f, d), 0.02))
+    w["w2"] = bf16_round(_normal(g("w2"), (d, f), 0.02))
+    for name in ("bq", "bv", "bo", "xbq", "xbo", "b2"):
+        w[name] = _normal(g(name), (d,), 0.01)
+    w["b1"] = _normal(g("b1"), (f,), 0.01)
+    for ln in ("ln1", "lnx", "ln2"):
+        if ln_random:
+            w[ln + "_g"] = (1.0 + _normal(g(ln + "_g"), (d,), 0.2)).astype(np.float32)
+            w[ln + "_b"] = _normal(g(ln + "_b"), (d,), 0.1)
+        else:
+            w[ln + "_g"] = _gamma(cfg, g(ln + "_g"), d)
+            w[ln + "_b"] = np.zeros(d, np.float32)
+    return w
+
+
+def decoder_weights(cfg: EncoderConfig, n_layer=None, n_vocab=None, n_text_ctx: int = N_TEXT_CTX,
+                    ln_random: bool = False) -> dict:
+    """All decoder weights of a decode step: "tok_embd" [n_vocab][d] (bf16 values; also the
+    output projection, Whisper ties them), "dec_pos" [n_text_ctx][d] float32, "layers" and
+    the final norm "lnf_g" / "lnf_b"."""
+    d = cfg.d_model
+    n_layer = cfg.n_layer if n_layer is None else n_layer
+    n_vocab = cfg.n_vocab if n_vocab is None else n_vocab
+    w = {"tok_embd": bf16_round(_normal(_rng(cfg, 1999, 0), (n_vocab, d), 0.02)),
+         "dec_pos": _normal(_rng(cfg, 1999, 1), (n_text_ctx, d), 0.02),
+         "layers": [decoder_layer_weights(cfg, l, ln_random) for l in range(n_layer)]}
+    if ln_random:
+        w["lnf_g"] = (1.0 + _normal(_rng(cfg, 1999, 2), (d,), 0.2)).astype(np.float32)
+        w["lnf_b"] = _normal(_rng(cfg, 1999, 3), (d,), 0.1)
+    else:
+        w["lnf_g"] = _gamma(cfg, _rng(cfg, 1999, 2), d)
+        w["lnf_b"] = np.zeros(d, np.float32)
+    return w
+
+
+def cross_kv_values(cfg: EncoderConfig, batch: int, n_ctx: int, n_layer=None, seed: int = 0) -> np.ndarray:
+    """Stand-in cross-attention keys and values for a decode step, in wh_prepare_cross's
+    layout: float32 (bf16 values) [n_layer][batch * n_ctx][2 d], K in columns 0..d-1 and V in
+    d..2d-1.  N(0, 0.5): about the spread of K = mem Wk^T for a unit-variance memory and
+    N(0, 0.02) weights at d = 384..1280."""
+    n_layer = cfg.n_layer if n_layer is None else n_layer
+    rng = np.random.Generator(np.random.PCG64([7 + cfg.index, 3000, seed]))
+    return bf16_round(_normal(rng, (n_layer, batch * n_ctx, 2 * cfg.d_model), 0.5))
