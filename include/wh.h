@@ -292,6 +292,71 @@ int wh_decode_attention(const wh_bf16 *q, const wh_bf16 *k, const wh_bf16 *v, in
                         wh_bf16 *out, void *workspace, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
+ * One decoder step for a batch of sequences ("whisper 0.9.0 API", model.nu, wh_decode_step:
+ * token tok at position pos, everything before it already in the KV cache, the logits left
+ * on the device; wk_addv_row adds the stored position row; setrow writes the token's key and
+ * value into the cache; wh_argmax is greedy decoding.  "How Audio Becomes Words", "The Full
+ * Stitched Circuit": a decoder block is causal self-attention, cross-attention into the
+ * encoder memory and a feed-forward, each behind its own LayerNorm and added to the residual;
+ * then a final LayerNorm and the output projection through the token embedding).
+ *
+ * For each sequence b, with t = tok[b] and p = pos[b]:
+ *   x = tok_embd[t] + pos_embd[p]
+ *   per layer l:  h = LN1(x); q = h Wq^T + bq; k = h Wk^T (no bias); v = h Wv^T + bv;
+ *                 kcache[l][b][p] = k, vcache[l][b][p] = v;
+ *                 x += attend(q, kcache[l][b][0..p], vcache[l][b][0..p]) Wo^T + bo
+ *                 h = LNx(x); x += attend(h Wxq^T + bxq, cross K_l, V_l of window b) Wxo^T + bxo
+ *                 h = LN2(x); x += GELU(h W1^T + b1) W2^T + b2
+ *   logits[b] = LNf(x) tok_embd^T;  next_tok[b] = the index of the first largest logit
+ * attend(q, K, V) is per head h: softmax(q_h K_h^T / sqrt(64)) V_h.  Rows of the self-attention
+ * caches past p are never read.  Tokens, positions, caches and logits stay on the device, so a
+ * decode loop needs no host round trip: the caller writes next_tok into tok and pos + 1 into
+ * pos (or records the step once in a CUDA graph and replays it).
+ *
+ *   tok, pos   device int32 [batch]: a token outside 0 .. n_vocab-1 or a position outside
+ *              0 .. n_text_ctx-1 is clamped into range (nothing outside a table or cache is
+ *              touched) and recorded as WH_EBOUNDS, which wh_status() then returns.
+ *   kcache, vcache  device bf16 [n_layer][batch][n_text_ctx][d_model]; row pos[b] of every
+ *              layer is written, rows 0 .. pos[b]-1 are read.
+ *   cross_kv   device bf16 [n_layer][batch * n_ctx][2 d_model]: wh_prepare_cross's output
+ *              (K in columns 0 .. d-1, V in d .. 2d-1), sequence b reading window b's rows.
+ *   logits     device float32 [batch][n_vocab];  next_tok  device int32 [batch] or NULL.
+ *   workspace  >= wh_decode_step_workspace(cfg, batch) bytes, 256-byte aligned, contents
+ *              need not be initialised; not shared by concurrent calls.
+ *   d_model a multiple of 128 in [128, 2048] with head_dim 64; d_ff a multiple of 128;
+ *   1 <= batch <= 256; 1 <= n_ctx <= 1500.  Matrices bf16 [out][in], vectors float32.
+ * Precision: bf16 operands on the tensor cores with fp32 accumulation, the residual stream in
+ * fp32, LayerNorm outputs, q / k / v, attention outputs and the caches in bf16.
+ * Errors: WH_EINVAL (null or misaligned pointer, shape out of range), WH_ENOSPC, WH_ECUDA.
+ * batch == 0 is a no-op.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+    int d_model, n_head, n_layer, d_ff, n_vocab, n_text_ctx;
+} wh_dec_config;
+typedef struct {
+    const float *ln1_g, *ln1_b;                  /* self-attention LayerNorm [d] */
+    const wh_bf16 *wq, *wk, *wv;                 /* [d][d] each (no k bias) */
+    const float *bq, *bv;                        /* [d] */
+    const wh_bf16 *wo;  const float *bo;         /* [d][d], [d] */
+    const float *lnx_g, *lnx_b;                  /* cross-attention LayerNorm [d] */
+    const wh_bf16 *xwq; const float *xbq;        /* cross query [d][d], [d] */
+    const wh_bf16 *xwo; const float *xbo;        /* cross output [d][d], [d] */
+    const float *ln2_g, *ln2_b;                  /* feed-forward LayerNorm [d] */
+    const wh_bf16 *w1;  const float *b1;         /* [d_ff][d], [d_ff] */
+    const wh_bf16 *w2;  const float *b2;         /* [d][d_ff], [d] */
+} wh_dec_layer_weights;
+typedef struct {
+    const wh_bf16 *tok_embd;                     /* [n_vocab][d]: embedding and output projection */
+    const float *pos;                            /* stored decoder positions [n_text_ctx][d] */
+    const wh_dec_layer_weights *layers;          /* HOST array [n_layer] */
+    const float *lnf_g, *lnf_b;                  /* final LayerNorm [d] */
+} wh_dec_weights;
+size_t wh_decode_step_workspace(const wh_dec_config *cfg, int batch);
+int wh_decode_step(const int *tok, const int *pos, int batch, const wh_dec_config *cfg, const wh_dec_weights *w,
+                   wh_bf16 *kcache, wh_bf16 *vcache, const wh_bf16 *cross_kv, int n_ctx, float *logits,
+                   int *next_tok, void *workspace, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
  * Status, errors, tracing
  * ------------------------------------------------------------------------------------ */
 

@@ -217,3 +217,37 @@ def test_shutdown_forgets_state_and_the_library_sets_up_again(L):
     assert L.wh_shutdown() == wh.WH_OK                       # idempotent
     if not torch.cuda.is_available():
         assert L.wh_frontend(FAKE, 480000, 1, 80, FAKE, FAKE, 256, None) == wh.WH_ENODEV
+
+
+def _dec_cfg(d=384, h=6, layers=1, ff=1536, vocab=1000, ctx=32):
+    return wh.wh_dec_config(d, h, layers, ff, vocab, ctx)
+
+
+@pytest.mark.parametrize("cfg", [(320, 5, 1, 1280, 100, 8), (384, 5, 1, 1536, 100, 8), (384, 6, -1, 1536, 100, 8),
+                                 (384, 6, 1, 100, 100, 8), (384, 6, 1, 1536, 0, 8), (384, 6, 1, 1536, 100, 0),
+                                 (4096, 64, 1, 4096, 100, 8)])
+def test_decode_step_rejects_unsupported_configs(L, cfg):
+    c = wh.wh_dec_config(*cfg)
+    w = wh.wh_dec_weights()
+    assert L.wh_decode_step_workspace(ctypes.byref(c), 4) == 0
+    assert L.wh_decode_step(FAKE, FAKE, 4, ctypes.byref(c), ctypes.byref(w), FAKE, FAKE, FAKE, 1500, FAKE, FAKE,
+                            FAKE, 1 << 40, None) == wh.WH_EINVAL
+
+
+def test_decode_step_rejects_bad_arguments_on_the_host(L):
+    c = _dec_cfg(layers=0)
+    w = wh.wh_dec_weights(FAKE, FAKE, None, FAKE, FAKE)
+    call = lambda batch=4, n_ctx=1500, tok=FAKE, ws=1 << 40, wp=w: L.wh_decode_step(
+        tok, FAKE, batch, ctypes.byref(c), ctypes.byref(wp), FAKE, FAKE, FAKE, n_ctx, FAKE, FAKE, FAKE, ws, None)
+    assert call(batch=0) == wh.WH_OK                                    # no-op
+    assert call(batch=257) == wh.WH_EINVAL                              # more sequences than one N tile
+    assert call(n_ctx=0) == wh.WH_EINVAL and call(n_ctx=1501) == wh.WH_EINVAL
+    assert call(tok=None) == wh.WH_EINVAL
+    assert call(tok=ctypes.c_void_p((1 << 20) + 2)) == wh.WH_EINVAL     # misaligned
+    assert call(wp=wh.wh_dec_weights()) == wh.WH_EINVAL                 # null weights
+    need = L.wh_decode_step_workspace(ctypes.byref(c), 4)
+    assert need > 0 and L.wh_decode_step_workspace(ctypes.byref(c), 257) == 0
+    assert call(ws=need - 1) == wh.WH_ENOSPC
+    c1 = _dec_cfg(layers=1)
+    assert L.wh_decode_step(FAKE, FAKE, 4, ctypes.byref(c1), ctypes.byref(w), FAKE, FAKE, FAKE, 1500, FAKE, FAKE,
+                            FAKE, 1 << 40, None) == wh.WH_EINVAL               # layers array missing

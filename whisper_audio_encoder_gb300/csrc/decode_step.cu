@@ -1,0 +1,584 @@
+// One decoder step for a batch of sequences ("whisper 0.9.0 API", model.nu, wh_decode_step:
+// token tok at position pos with everything before it already in the KV cache, the logits
+// left on the device; wk_addv_row: the stored position row is added; setrow: the token's
+// key and value are written into the cache; wh_argmax: greedy decoding on the device.
+// "How Audio Becomes Words", "The Full Stitched Circuit": each decoder block is causal
+// self-attention, cross-attention into the encoder memory and a feed-forward, each behind
+// its own LayerNorm and added to the residual; a final norm and the output projection
+// through the token embedding follow.)
+//
+// Per step: k_dec_embed, then per layer LN -> QKV (q out, k / v appended at row pos of the
+// caches) -> one-query self-attention over rows 0..pos -> out_proj + residual -> LN -> cross
+// q -> one-query cross-attention over the layer's cached K/V -> cross out + residual -> LN ->
+// fc1 + GELU -> fc2 + residual; final LN -> logits (+ argmax) -> next token.
+//
+// k_dec_gemm: the step's dense layers have one row per sequence (a few to a few hundred), so
+// they stream their weights once and are bound by HBM.  On the tensor cores the weights are
+// the M operand: a CTA computes D[128 features][B tokens] = W[n0 .. n0+127][K] X[B][K]^T with
+// tcgen05.mma (M = 128, N = B rounded up to 16, K = 16), both operands K-major from a TMA ring,
+// the accumulator in TMEM (lane = feature, column = token).  K is split across CTAs so that
+// every SM streams weights; each split writes its partial tile and the last split of a tile
+// to finish (an atomic ticket, no block waits for another) adds the partials in split order
+// and applies the epilogue, so the result does not depend on timing.
+#include "common.cuh"
+#include "internal.h"
+
+namespace wh {
+
+namespace {
+
+constexpr int SK_THREADS = 192;   // warp 0 TMA, warp 1 TMEM + MMA, warps 2..5 epilogue
+constexpr int SK_STAGES = 4;
+constexpr int SK_BK = 64;
+constexpr int SK_W_BYTES = 128 * SK_BK * 2;   // one k-block of 128 weight rows
+constexpr int SK_MAX_SPLITS = 16;
+constexpr int SK_MAX_B = 256;
+
+enum SkMode { SK_QKV = 0, SK_BF16 = 1, SK_GELU = 2, SK_RESID = 3, SK_LOGITS = 4 };
+
+struct SkArgs {
+    int N, seg_n, num_kb, kb_per, B, B_pad, x_bytes, stage_bytes, tmem_cols;
+    const float *bias[3];
+    void *out[3];
+    int cap;                    // SK_QKV: cache rows per sequence
+    const int *pos;             // SK_QKV: cache row of each sequence (already in range)
+    float *part;                // [splits][B][N] partial sums (gridDim.y > 1)
+    int *ticket;                // [tiles], zero on entry and on exit
+    unsigned long long *amax;   // SK_LOGITS: per-sequence (logit key, ~index), zero on entry
+    DevCtl ctl;
+};
+struct SkMaps {
+    CUtensorMap w[3];
+};
+
+// Order-preserving float -> uint32 (larger float, larger key).
+__device__ __forceinline__ uint32_t ord_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// The finished value of output feature n for sequence b.
+template <int MODE>
+__device__ __forceinline__ void sk_finish(const SkArgs &p, int b, int n, float bias, float v,
+                                          unsigned long long &best) {
+    v += bias;
+    if constexpr (MODE == SK_QKV) {
+        const int seg = n / p.seg_n, nin = n - seg * p.seg_n;
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out[seg]);
+        const long long row = seg == 0 ? b : (long long)b * p.cap + __ldg(p.pos + b);
+        o[row * p.seg_n + nin] = __float2bfloat16_rn(v);
+    } else if constexpr (MODE == SK_BF16 || MODE == SK_GELU) {
+        if constexpr (MODE == SK_GELU) v = gelu_erf(v);
+        static_cast<__nv_bfloat16 *>(p.out[0])[(long long)b * p.N + n] = __float2bfloat16_rn(v);
+    } else if constexpr (MODE == SK_RESID) {
+        float *x = static_cast<float *>(p.out[0]) + (long long)b * p.N + n;
+        *x += v;
+    } else {  // SK_LOGITS
+        if (n < p.N) {
+            static_cast<float *>(p.out[0])[(long long)b * p.N + n] = v;
+            best = ((unsigned long long)ord_key(v) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)n);
+        } else {
+            best = 0ull;
+        }
+    }
+}
+
+// Largest key over the warp (the logit, then the lowest index).
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__ SkMaps tw,
+                                                         const __grid_constant__ CUtensorMap tx, const SkArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + SK_STAGES * p.stage_bytes);
+    uint64_t *empty = full + SK_STAGES;
+    uint64_t *accf = empty + SK_STAGES;
+    uint64_t *drain = accf + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ int last_split, epi_fail;
+    __shared__ unsigned long long cta_best[SK_MAX_B];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x, split = blockIdx.y, splits = gridDim.y;
+    const int n0 = tile * 128, seg = n0 / p.seg_n, nin0 = n0 - seg * p.seg_n;
+    const int kb0 = split * p.kb_per, kb1 = min(p.num_kb, kb0 + p.kb_per);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SK_STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(accf, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        epi_fail = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tw.w[seg]);
+        tma_prefetch_desc(&tx);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        int stage = 0;
+        uint32_t phase = 0, issued = 0, last_parity = 0;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (*abort_flag || !mbar_wait(empty + stage, phase ^ 1u, p.ctl)) {
+                *abort_flag = 1;
+                break;
+            }
+            uint8_t *sw = smem + stage * p.stage_bytes;
+            mbar_arrive_expect_tx(full + stage, (uint32_t)(SK_W_BYTES + p.x_bytes));
+            tma_load_2d(sw, &tw.w[seg], full + stage, kb * SK_BK, nin0);
+            tma_load_2d(sw + SK_W_BYTES, &tx, full + stage, kb * SK_BK, 0);
+            issued |= 1u << stage;
+            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == SK_STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        // no copy of this CTA may still be in flight when it leaves
+        for (int s = 0; s < SK_STAGES; ++s)
+            if ((issued >> s) & 1u) mbar_wait(full + s, (last_parity >> s) & 1u, p.ctl);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        const uint32_t idesc = idesc_bf16_f32(128, p.B_pad);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (*abort_flag || !mbar_wait(full + stage, phase, p.ctl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
+            const uint64_t ad = sdesc_sw128(sa), bd = sdesc_sw128(sa + SK_W_BYTES);
+#pragma unroll
+            for (int k = 0; k < SK_BK / 16; ++k)
+                umma_bf16(tmem_base, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
+                          (kb > kb0 || k > 0) ? 1u : 0u);
+            umma_commit(empty + stage);
+            if (++stage == SK_STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) *abort_flag = 1;
+        umma_commit(ok ? accf : drain);
+        if (!ok) mbar_wait(drain, 0, p.ctl);   // every MMA issued so far has completed
+    } else if (warp >= 2) {
+        // ---------------- epilogue: feature n = n0 + 32 q + lane, every sequence ----------------
+        const int q = warp & 3, n = n0 + 32 * q + lane;
+        if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(accf, 0, p.ctl)) && lane == 0) epi_fail = 1;
+        float bias = 0.0f;
+        if (MODE != SK_LOGITS) {
+            const int sg = n / p.seg_n;
+            const float *bp = p.bias[sg];
+            if (bp != nullptr) bias = __ldg(bp + (n - sg * p.seg_n));
+        }
+        if (MODE == SK_LOGITS)
+            for (int b = threadIdx.x - 64; b < p.B; b += 128) cta_best[b] = 0ull;
+        epi_bar();
+        // one verdict for all four epilogue warps, so that they all reach the same barriers
+        const bool ok = epi_fail == 0;
+        if (!ok) *abort_flag = 1;
+        if (ok) {
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16);
+            for (int c = 0; c < p.B_pad; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(tbase + (uint32_t)c, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int b = c + j;
+                    if (b >= p.B) break;
+                    const float v = __uint_as_float(r[j]);
+                    if (splits > 1) {
+                        if (n < p.N) __stcg(p.part + ((long long)split * p.B + b) * p.N + n, v);
+                    } else {
+                        unsigned long long best = 0ull;
+                        sk_finish<MODE>(p, b, n, bias, v, best);
+                        if constexpr (MODE == SK_LOGITS) {
+                            best = warp_max_u64(best);
+                            if (lane == 0) atomicMax(cta_best + b, best);
+                        }
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        if (ok && splits > 1) {
+            // the last split of this tile to finish adds the partials in split order
+            __threadfence();
+            epi_bar();
+            if (threadIdx.x == 64) last_split = atomicAdd(p.ticket + tile, 1) == splits - 1;
+            epi_bar();
+            if (last_split) {
+                __threadfence();
+                for (int b = 0; b < p.B; ++b) {
+                    float v = 0.0f;
+                    if (n < p.N)
+                        for (int s = 0; s < splits; ++s) v += __ldcg(p.part + ((long long)s * p.B + b) * p.N + n);
+                    unsigned long long best = 0ull;
+                    if (n < p.N || MODE == SK_LOGITS) sk_finish<MODE>(p, b, n, bias, v, best);
+                    if constexpr (MODE == SK_LOGITS) {
+                        best = warp_max_u64(best);
+                        if (lane == 0) atomicMax(cta_best + b, best);
+                    }
+                }
+                if (threadIdx.x == 64) p.ticket[tile] = 0;   // ready for the next launch
+            }
+        }
+        if (MODE == SK_LOGITS) {
+            epi_bar();
+            for (int b = threadIdx.x - 64; b < p.B; b += 128)
+                if (cta_best[b] != 0ull) atomicMax(p.amax + b, cta_best[b]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+    }
+}
+
+// x[b] = tok_embd[tok[b]] + dec_pos[pos[b]] (fp32), the cache row and self-attention key count
+// of every sequence, and the argmax keys cleared.  A token or position outside its table is
+// clamped into it and reported as WH_EBOUNDS: nothing outside the tables or caches is read or
+// written.
+__global__ void __launch_bounds__(256) k_dec_embed(const int *__restrict__ tok, const int *__restrict__ pos,
+                                                   const __nv_bfloat16 *__restrict__ emb,
+                                                   const float *__restrict__ dpos, int d, int n_vocab, int cap,
+                                                   float *__restrict__ x, int *__restrict__ pos_c,
+                                                   int *__restrict__ n_self, unsigned long long *__restrict__ amax,
+                                                   int *status) {
+    const int b = blockIdx.x;
+    const int t_in = __ldg(tok + b), p_in = __ldg(pos + b);
+    const int t = min(max(t_in, 0), n_vocab - 1), ps = min(max(p_in, 0), cap - 1);
+    if (threadIdx.x == 0) {
+        if (t != t_in || ps != p_in) atomicCAS(status, 0, WH_EBOUNDS);
+        pos_c[b] = ps;
+        n_self[b] = ps + 1;
+        amax[b] = 0ull;
+    }
+    const uint4 *e = reinterpret_cast<const uint4 *>(emb + (long long)t * d);
+    const float4 *pp = reinterpret_cast<const float4 *>(dpos + (long long)ps * d);
+    float4 *xo = reinterpret_cast<float4 *>(x + (long long)b * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+        const uint4 u = __ldg(e + i);
+        const float4 p0 = __ldg(pp + 2 * i), p1 = __ldg(pp + 2 * i + 1);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f[2 * j] = __uint_as_float(w[j] << 16);
+            f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+        }
+        xo[2 * i] = make_float4(f[0] + p0.x, f[1] + p0.y, f[2] + p0.z, f[3] + p0.w);
+        xo[2 * i + 1] = make_float4(f[4] + p1.x, f[5] + p1.y, f[6] + p1.z, f[7] + p1.w);
+    }
+}
+
+__global__ void k_dec_argmax_out(const unsigned long long *__restrict__ amax, int batch, int *__restrict__ next) {
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < batch; b += gridDim.x * blockDim.x)
+        next[b] = (int)(0xffffffffu - (uint32_t)(amax[b] & 0xffffffffull));
+}
+
+int sk_b_pad(int batch) { return (batch + 15) / 16 * 16; }
+int sk_stage_bytes(int b_pad) { return SK_W_BYTES + (b_pad * 128 + 1023) / 1024 * 1024; }
+int sk_smem_bytes(int b_pad) { return SK_STAGES * sk_stage_bytes(b_pad) + 1024 + 128; }
+
+template <int MODE>
+int sk_set_attr() {
+    return cudaFuncSetAttribute(k_dec_gemm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                sk_smem_bytes(SK_MAX_B)) == cudaSuccess
+               ? WH_OK
+               : WH_ECUDA;
+}
+
+}  // namespace
+
+int dec_gemm_prepare() {
+    return sk_set_attr<SK_QKV>() | sk_set_attr<SK_BF16>() | sk_set_attr<SK_GELU>() | sk_set_attr<SK_RESID>() |
+           sk_set_attr<SK_LOGITS>();
+}
+
+size_t dec_gemm_partials(int batch, int n_max) { return (size_t)SK_MAX_SPLITS * batch * n_max * sizeof(float); }
+
+// y = epilogue(x[batch][K] w[N][K]^T + bias) for one of the SkMode epilogues.  w may be up to
+// three segments of seg_n rows (QKV); N = segments x seg_n, or any N for the logits.
+int dec_gemm_launch(int mode, const void *x, int batch, int K, const void *const w[3], int seg_n, int N,
+                    const float *const bias[3], void *const out[3], int cap, const int *pos, float *part,
+                    int *ticket, unsigned long long *amax, const DevCtl &ctl, int num_sms, cudaStream_t s) {
+    if (batch < 1 || batch > SK_MAX_B || K < 8 || K % 8 != 0 || N < 1 || seg_n < 1) return WH_EINVAL;
+    if (mode != SK_LOGITS && (seg_n % 128 != 0 || N % seg_n != 0 || N / seg_n > 3)) return WH_EINVAL;
+    const int b_pad = sk_b_pad(batch);
+    SkArgs a;
+    a.N = N;
+    a.seg_n = mode == SK_LOGITS ? N : seg_n;
+    a.num_kb = (K + SK_BK - 1) / SK_BK;
+    a.B = batch;
+    a.B_pad = b_pad;
+    a.x_bytes = b_pad * 128;
+    a.stage_bytes = sk_stage_bytes(b_pad);
+    a.tmem_cols = b_pad <= 32 ? 32 : (b_pad <= 64 ? 64 : (b_pad <= 128 ? 128 : 256));
+    for (int i = 0; i < 3; ++i) {
+        a.bias[i] = bias ? bias[i] : nullptr;
+        a.out[i] = out[i];
+    }
+    a.cap = cap;
+    a.pos = pos;
+    a.part = part;
+    a.ticket = ticket;
+    a.amax = amax;
+    a.ctl = ctl;
+    SkMaps tw;
+    const int nseg = mode == SK_LOGITS ? 1 : N / seg_n;
+    for (int i = 0; i < 3; ++i)
+        if (int rc = make_tmap_bf16(&tw.w[i], w[i < nseg ? i : 0], a.seg_n, K, K, 128)) return rc;
+    CUtensorMap tx;
+    if (int rc = make_tmap_bf16(&tx, x, batch, K, K, b_pad)) return rc;
+    const int tiles = (N + 127) / 128;
+    // split K so that about two CTAs per SM stream weights; every split gets >= 1 k-block
+    int splits = 1;
+    if (mode != SK_LOGITS) {
+        const int target = 2 * num_sms;
+        splits = (target + tiles - 1) / tiles;
+        splits = splits < 1 ? 1 : (splits > SK_MAX_SPLITS ? SK_MAX_SPLITS : splits);
+        splits = splits > a.num_kb ? a.num_kb : splits;
+    }
+    a.kb_per = (a.num_kb + splits - 1) / splits;
+    splits = (a.num_kb + a.kb_per - 1) / a.kb_per;
+    if (tiles > 65535 * 16) return WH_EINVAL;
+    const dim3 grid(tiles, splits);
+    const int smem = sk_smem_bytes(b_pad);
+    cudaError_t e;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = dim3(SK_THREADS);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    switch (mode) {
+        case SK_QKV: e = cudaLaunchKernelEx(&lc, k_dec_gemm<SK_QKV>, tw, tx, a); break;
+        case SK_BF16: e = cudaLaunchKernelEx(&lc, k_dec_gemm<SK_BF16>, tw, tx, a); break;
+        case SK_GELU: e = cudaLaunchKernelEx(&lc, k_dec_gemm<SK_GELU>, tw, tx, a); break;
+        case SK_RESID: e = cudaLaunchKernelEx(&lc, k_dec_gemm<SK_RESID>, tw, tx, a); break;
+        case SK_LOGITS: e = cudaLaunchKernelEx(&lc, k_dec_gemm<SK_LOGITS>, tw, tx, a); break;
+        default: return WH_EINVAL;
+    }
+    count_launch();
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
+}
+
+int dec_embed_launch(const int *tok, const int *pos, const void *emb, const float *dpos, int d, int n_vocab, int cap,
+                     int batch, float *x, int *pos_c, int *n_self, unsigned long long *amax, const DevCtl &ctl,
+                     cudaStream_t s) {
+    k_dec_embed<<<batch, 256, 0, s>>>(tok, pos, static_cast<const __nv_bfloat16 *>(emb), dpos, d, n_vocab, cap, x,
+                                      pos_c, n_self, amax, ctl.status);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
+}
+
+int dec_argmax_launch(const unsigned long long *amax, int batch, int *next, cudaStream_t s) {
+    k_dec_argmax_out<<<(batch + 255) / 256, 256, 0, s>>>(amax, batch, next);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
+}
+
+}  // namespace wh
+
+// ---------------------------------------------------------------------------------------
+// wh_decode_step: argument checks, workspace layout and the step's launch sequence
+// ---------------------------------------------------------------------------------------
+namespace wh {
+namespace {
+
+constexpr int DEC_MAX_CROSS = 1500;   // encoder positions
+
+size_t up256d(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct DecLayout {
+    size_t x, xn, q, ao, h, pos_c, n_self, amax, part, ticket, da, total;
+    size_t ticket_bytes;
+};
+
+DecLayout dec_layout(const wh_dec_config *c, int batch) {
+    const size_t B = batch, d = c->d_model, f = c->d_ff;
+    const int n_max = 3 * c->d_model > c->d_ff ? 3 * c->d_model : c->d_ff;
+    const int keys = c->n_text_ctx > DEC_MAX_CROSS ? c->n_text_ctx : DEC_MAX_CROSS;
+    DecLayout L;
+    size_t off = 0;
+    L.x = off;      off += up256d(B * d * 4);
+    L.xn = off;     off += up256d(B * d * 2);
+    L.q = off;      off += up256d(B * d * 2);
+    L.ao = off;     off += up256d(B * d * 2);
+    L.h = off;      off += up256d(B * f * 2);
+    L.pos_c = off;  off += up256d(B * 4);
+    L.n_self = off; off += up256d(B * 4);
+    L.amax = off;   off += up256d(B * 8);
+    L.part = off;   off += up256d(dec_gemm_partials(batch, n_max));
+    L.ticket_bytes = (size_t)((n_max + 127) / 128) * 4;
+    L.ticket = off; off += up256d(L.ticket_bytes);
+    L.da = off;     off += up256d(decode_attention_workspace(batch, c->n_head, keys));
+    L.total = off;
+    return L;
+}
+
+int check_dec_config(const wh_dec_config *c) {
+    if (!c) return WH_EINVAL;
+    if (c->d_model < 128 || c->d_model > 2048 || c->d_model % 128 != 0) return WH_EINVAL;
+    if (c->n_head < 1 || c->d_model != 64 * c->n_head) return WH_EINVAL;
+    if (c->n_layer < 0 || c->d_ff < 128 || c->d_ff % 128 != 0 || c->d_ff > 16384) return WH_EINVAL;
+    if (c->n_vocab < 1 || c->n_vocab > (1 << 24) || c->n_text_ctx < 1 || c->n_text_ctx > 65536) return WH_EINVAL;
+    return WH_OK;
+}
+
+bool al(const void *p, size_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_dec_weights(const wh_dec_config *c, const wh_dec_weights *w) {
+    if (!w || !al(w->tok_embd, 16) || !al(w->pos, 16) || !al(w->lnf_g, 16) || !al(w->lnf_b, 16)) return WH_EINVAL;
+    if (c->n_layer > 0 && !w->layers) return WH_EINVAL;
+    for (int l = 0; l < c->n_layer; ++l) {
+        const wh_dec_layer_weights &L = w->layers[l];
+        const void *need[] = {L.ln1_g, L.ln1_b, L.wq, L.wk, L.wv, L.bq, L.bv, L.wo, L.bo, L.lnx_g, L.lnx_b,
+                              L.xwq, L.xbq, L.xwo, L.xbo, L.ln2_g, L.ln2_b, L.w1, L.b1, L.w2, L.b2};
+        for (const void *p : need)
+            if (!al(p, 16)) return WH_EINVAL;
+    }
+    return WH_OK;
+}
+
+}  // namespace
+}  // namespace wh
+
+using namespace wh;
+
+extern "C" size_t wh_decode_step_workspace(const wh_dec_config *cfg, int batch) {
+    if (check_dec_config(cfg) != WH_OK || batch < 1 || batch > SK_MAX_B) return 0;
+    return dec_layout(cfg, batch).total;
+}
+
+extern "C" int wh_decode_step(const int *tok, const int *pos, int batch, const wh_dec_config *cfg,
+                              const wh_dec_weights *w, wh_bf16 *kcache, wh_bf16 *vcache, const wh_bf16 *cross_kv,
+                              int n_ctx, float *logits, int *next_tok, void *workspace, size_t ws_bytes,
+                              void *stream) {
+    if (int rc = check_dec_config(cfg)) return rc;
+    if (batch < 0 || batch > SK_MAX_B || n_ctx < 1 || n_ctx > DEC_MAX_CROSS) return WH_EINVAL;
+    if (batch == 0) return WH_OK;
+    if (!al(tok, 4) || !al(pos, 4) || !al(logits, 16) || !al(workspace, 256) || (next_tok && !al(next_tok, 4)))
+        return WH_EINVAL;
+    if (cfg->n_layer > 0 && (!al(kcache, 16) || !al(vcache, 16) || !al(cross_kv, 16))) return WH_EINVAL;
+    if (int rc = check_dec_weights(cfg, w)) return rc;
+    const DecLayout L = dec_layout(cfg, batch);
+    if (ws_bytes < L.total) return WH_ENOSPC;
+    DevCtl ctl;
+    int num_sms = 0;
+    if (int rc = device_ctl(&ctl, &num_sms)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    const int d = cfg->d_model, f = cfg->d_ff, H = cfg->n_head, cap = cfg->n_text_ctx, V = cfg->n_vocab;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *x = reinterpret_cast<float *>(ws + L.x);
+    void *xn = ws + L.xn, *q = ws + L.q, *ao = ws + L.ao, *hb = ws + L.h;
+    int *pos_c = reinterpret_cast<int *>(ws + L.pos_c), *n_self = reinterpret_cast<int *>(ws + L.n_self);
+    unsigned long long *amax = reinterpret_cast<unsigned long long *>(ws + L.amax);
+    float *part = reinterpret_cast<float *>(ws + L.part);
+    int *ticket = reinterpret_cast<int *>(ws + L.ticket);
+    void *da = ws + L.da;
+    const size_t layer_cache = (size_t)batch * cap * d;
+    const size_t layer_cross = (size_t)batch * n_ctx * 2 * d;
+    int rc;
+
+    trace_begin(TR_DEC_OTHER, s);
+    if (cudaMemsetAsync(ticket, 0, L.ticket_bytes, s) != cudaSuccess) return WH_ECUDA;
+    rc = dec_embed_launch(tok, pos, w->tok_embd, w->pos, d, V, cap, batch, x, pos_c, n_self, amax, ctl, s);
+    trace_end(TR_DEC_OTHER, s, 0.0, (double)batch * d * 10.0);
+    if (rc) return rc;
+
+    auto gemm = [&](int mode, const void *a, int K, const void *w0, const void *w1, const void *w2, int seg_n, int N,
+                    const float *b0, const float *b1, const float *b2, void *o0, void *o1, void *o2) {
+        const void *wv[3] = {w0, w1 ? w1 : w0, w2 ? w2 : w0};
+        const float *bv[3] = {b0, b1, b2};
+        void *ov[3] = {o0, o1, o2};
+        trace_begin(TR_DEC_GEMM, s);
+        const int r = dec_gemm_launch(mode, a, batch, K, wv, seg_n, N, bv, ov, cap, pos_c, part, ticket, amax, ctl,
+                                      num_sms, s);
+        trace_end(TR_DEC_GEMM, s, 2.0 * batch * (double)N * K, 2.0 * (double)N * K + 2.0 * batch * (double)K);
+        return r;
+    };
+    auto ln = [&](const float *g, const float *b) {
+        trace_begin(TR_DEC_OTHER, s);
+        const int r = layernorm_launch(x, batch, d, g, b, xn, 1, s);
+        trace_end(TR_DEC_OTHER, s, 0.0, (double)batch * d * 6.0);
+        return r;
+    };
+    auto attend = [&](const void *qp, const void *kp, const void *vp, long long row_stride, long long seq_stride,
+                      const int *nk, int max_keys) {
+        trace_begin(TR_DEC_ATTN, s);
+        const int r = decode_attention_launch(qp, kp, vp, row_stride, seq_stride, nk, max_keys, batch, H, ao, da, ctl,
+                                              num_sms, s);
+        trace_end(TR_DEC_ATTN, s, 4.0 * batch * (double)max_keys * d, 4.0 * batch * (double)max_keys * d);
+        return r;
+    };
+
+    for (int l = 0; l < cfg->n_layer; ++l) {
+        const wh_dec_layer_weights &Lw = w->layers[l];
+        wh_bf16 *kc = kcache + (size_t)l * layer_cache, *vc = vcache + (size_t)l * layer_cache;
+        const wh_bf16 *ckv = cross_kv + (size_t)l * layer_cross;
+        // causal self-attention: this token's k / v go to row pos of the caches, then its
+        // query attends over rows 0 .. pos
+        if ((rc = ln(Lw.ln1_g, Lw.ln1_b))) return rc;
+        if ((rc = gemm(SK_QKV, xn, d, Lw.wq, Lw.wk, Lw.wv, d, 3 * d, Lw.bq, nullptr, Lw.bv, q, kc, vc))) return rc;
+        if ((rc = attend(q, kc, vc, d, (long long)cap * d, n_self, cap))) return rc;
+        if ((rc = gemm(SK_RESID, ao, d, Lw.wo, nullptr, nullptr, d, d, Lw.bo, nullptr, nullptr, x, nullptr, nullptr)))
+            return rc;
+        // cross-attention into the encoder memory (keys / values cached once per clip)
+        if ((rc = ln(Lw.lnx_g, Lw.lnx_b))) return rc;
+        if ((rc = gemm(SK_BF16, xn, d, Lw.xwq, nullptr, nullptr, d, d, Lw.xbq, nullptr, nullptr, q, nullptr, nullptr)))
+            return rc;
+        if ((rc = attend(q, ckv, ckv + d, 2LL * d, (long long)n_ctx * 2 * d, nullptr, n_ctx))) return rc;
+        if ((rc = gemm(SK_RESID, ao, d, Lw.xwo, nullptr, nullptr, d, d, Lw.xbo, nullptr, nullptr, x, nullptr,
+                       nullptr)))
+            return rc;
+        // feed-forward
+        if ((rc = ln(Lw.ln2_g, Lw.ln2_b))) return rc;
+        if ((rc = gemm(SK_GELU, xn, d, Lw.w1, nullptr, nullptr, f, f, Lw.b1, nullptr, nullptr, hb, nullptr, nullptr)))
+            return rc;
+        if ((rc = gemm(SK_RESID, hb, f, Lw.w2, nullptr, nullptr, d, d, Lw.b2, nullptr, nullptr, x, nullptr, nullptr)))
+            return rc;
+    }
+    // final norm, logits through the token embedding, greedy token
+    if ((rc = ln(w->lnf_g, w->lnf_b))) return rc;
+    if ((rc = gemm(SK_LOGITS, xn, d, w->tok_embd, nullptr, nullptr, V, V, nullptr, nullptr, nullptr, logits, nullptr,
+                   nullptr)))
+        return rc;
+    if (next_tok) {
+        trace_begin(TR_DEC_OTHER, s);
+        rc = dec_argmax_launch(amax, batch, next_tok, s);
+        trace_end(TR_DEC_OTHER, s, 0.0, (double)batch * 12.0);
+    }
+    return rc;
+}

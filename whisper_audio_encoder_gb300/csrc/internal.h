@@ -72,14 +72,19 @@ int cast_bf16_launch(const float *x, long long n, void *y, cudaStream_t s);
 int pack_conv_weight_launch(const void *w, int c_out, int c_in, void *wp, cudaStream_t s);
 int selftest_timeout_launch(const DevCtl &ctl, cudaStream_t s);
 
+// ---- decoder step (decode_step.cu) ---------------------------------------------------------
+int dec_gemm_prepare();   // once per device: shared-memory attributes of the step's GEMMs
+
 // ---- per-device set-up (wh_api.cu): constant tables and status word, once per device ----
 int device_setup();
+int device_ctl(DevCtl *ctl, int *num_sms);     // the current device's control block and SM count
 
 // ---- tracing (wh_api.cu) ------------------------------------------------------------------
 // Kernel classes for the per-kernel timing.
 enum TraceClass {
     TR_FRONTEND = 0, TR_STEM_PREP, TR_GEMM, TR_ATTN, TR_LAYERNORM,
-    TR_GEMM_CONV, TR_GEMM_QKV, TR_GEMM_OUT, TR_GEMM_FC1, TR_GEMM_FC2, TR_CROSS_PREP, TR_GEMM_CROSS, TR_DEC_ATTN, TR_RESAMPLE, TR_NCLASS
+    TR_GEMM_CONV, TR_GEMM_QKV, TR_GEMM_OUT, TR_GEMM_FC1, TR_GEMM_FC2, TR_CROSS_PREP, TR_GEMM_CROSS, TR_DEC_ATTN, TR_RESAMPLE,
+    TR_DEC_GEMM, TR_DEC_OTHER, TR_NCLASS
 };
 void trace_begin(int cls, cudaStream_t s);
 void trace_end(int cls, cudaStream_t s, double flops, double bytes);

@@ -59,6 +59,7 @@ int ensure_device(DevState **out) {
         if (int rc = gemm_prepare(st.num_sms)) return rc;
         if (int rc = attention_prepare()) return rc;
         if (int rc = resample_prepare()) return rc;
+        if (int rc = dec_gemm_prepare()) return rc;
         st.status = static_cast<int *>(p);
         st.ready = true;
     }
@@ -85,7 +86,7 @@ struct TraceRec {
 const char *const kTraceNames[TR_NCLASS] = {"frontend", "stem_prep", "gemm",       "attention",
                                              "layernorm", "gemm_conv", "gemm_qkv",   "gemm_out",
                                              "gemm_fc1",  "gemm_fc2",  "cross_prep", "gemm_cross",
-                                             "decode_attention", "resample"};
+                                             "decode_attention", "resample", "dec_gemm", "dec_other"};
 std::mutex g_tr_mu;
 bool g_tr_on = false;
 std::vector<TraceRec> g_tr;
@@ -197,6 +198,8 @@ int device_setup() {
     DevState *st;
     return ensure_device(&st);
 }
+
+int device_ctl(DevCtl *ctl, int *num_sms) { return frontend_ctl(ctl, num_sms); }
 
 void trace_begin(int cls, cudaStream_t s) {
     std::lock_guard<std::mutex> lk(g_tr_mu);

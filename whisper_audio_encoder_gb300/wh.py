@@ -39,6 +39,24 @@ class wh_cross_weights(ctypes.Structure):
     _fields_ = [("wk", ctypes.POINTER(_p)), ("wv", ctypes.POINTER(_p)), ("bv", ctypes.POINTER(_p))]
 
 
+class wh_dec_config(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("n_head", ctypes.c_int), ("n_layer", ctypes.c_int),
+                ("d_ff", ctypes.c_int), ("n_vocab", ctypes.c_int), ("n_text_ctx", ctypes.c_int)]
+
+
+_DEC_LAYER_FIELDS = ["ln1_g", "ln1_b", "wq", "wk", "wv", "bq", "bv", "wo", "bo", "lnx_g", "lnx_b", "xwq", "xbq",
+                     "xwo", "xbo", "ln2_g", "ln2_b", "w1", "b1", "w2", "b2"]
+
+
+class wh_dec_layer_weights(ctypes.Structure):
+    _fields_ = [(n, _p) for n in _DEC_LAYER_FIELDS]
+
+
+class wh_dec_weights(ctypes.Structure):
+    _fields_ = [("tok_embd", _p), ("pos", _p), ("layers", ctypes.POINTER(wh_dec_layer_weights)),
+                ("lnf_g", _p), ("lnf_b", _p)]
+
+
 class wh_trace_stat(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double),
                 ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
@@ -78,6 +96,10 @@ def lib():
         "wh_decode_attention_workspace": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
         "wh_decode_attention": (ctypes.c_int, [_p, _p, _p, ctypes.c_int64, ctypes.c_int64, _p, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, _p, _p, ctypes.c_size_t, _p]),
+        "wh_decode_step_workspace": (ctypes.c_size_t, [ctypes.POINTER(wh_dec_config), ctypes.c_int]),
+        "wh_decode_step": (ctypes.c_int, [_p, _p, ctypes.c_int, ctypes.POINTER(wh_dec_config),
+                                          ctypes.POINTER(wh_dec_weights), _p, _p, _p, ctypes.c_int, _p, _p, _p,
+                                          ctypes.c_size_t, _p]),
         "wh_frontend_windows": (ctypes.c_int64, [ctypes.c_int64]),
         "wh_frontend_long": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int, _p, _p, ctypes.c_size_t, _p]),
         "wh_resample_length": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int]),
@@ -250,8 +272,8 @@ def wh_trace_enable(on: bool):
 
 
 def wh_trace_read():
-    arr = (wh_trace_stat * 16)()
-    n = lib().wh_trace_read(arr, 16)
+    arr = (wh_trace_stat * 32)()
+    n = lib().wh_trace_read(arr, 32)
     if n < 0:
         raise WhError(-n, "wh_trace_read")
     return {arr[i].name.decode(): {"launches": arr[i].launches, "total_ms": arr[i].total_ms,
@@ -500,3 +522,57 @@ class Pipeline:
     def destroy(self):
         for g in self.graphs:
             g.destroy()
+
+
+# ---------------------------------------------------------------------------------------
+# Decoder step (wh_decode_step): device weights, self-attention caches, workspace
+# ---------------------------------------------------------------------------------------
+class Decoder:
+    """Holds a decoder's weights and its self-attention caches on the device and calls
+    wh_decode_step.  `weights` is a dict as produced by synth.decoder_weights: "tok_embd"
+    [n_vocab][d] and matrices bf16-representable float32, vectors float32, "layers" a list of
+    per-block dicts.  The caches are bf16 [n_layer][batch][n_text_ctx][d_model]."""
+
+    def __init__(self, n_head: int, weights: dict, batch: int, device="cuda"):
+        import torch
+        self.device = torch.device(device)
+        self._keep = []
+
+        def put(a, dtype):
+            t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dtype).to(self.device)
+            self._keep.append(t)
+            return t.data_ptr()
+
+        n_vocab, d = weights["tok_embd"].shape
+        n_text_ctx = weights["dec_pos"].shape[0]
+        n_layer = len(weights["layers"])
+        d_ff = weights["layers"][0]["w1"].shape[0] if n_layer else 4 * d
+        self.batch = batch
+        self.c_cfg = wh_dec_config(d, n_head, n_layer, d_ff, n_vocab, n_text_ctx)
+        self._layers = (wh_dec_layer_weights * max(1, n_layer))()
+        for i, lw in enumerate(weights["layers"]):
+            L = self._layers[i]
+            for name in _DEC_LAYER_FIELDS:
+                is_mat = name in ("wq", "wk", "wv", "wo", "xwq", "xwo", "w1", "w2")
+                setattr(L, name, put(lw[name], torch.bfloat16 if is_mat else torch.float32))
+        self.c_w = wh_dec_weights(put(weights["tok_embd"], torch.bfloat16), put(weights["dec_pos"], torch.float32),
+                                  ctypes.cast(self._layers, ctypes.POINTER(wh_dec_layer_weights)),
+                                  put(weights["lnf_g"], torch.float32), put(weights["lnf_b"], torch.float32))
+        shape = (max(1, n_layer), batch, n_text_ctx, d)
+        self.kcache = torch.zeros(shape, dtype=torch.bfloat16, device=self.device)
+        self.vcache = torch.zeros(shape, dtype=torch.bfloat16, device=self.device)
+        self.logits = torch.empty(batch, n_vocab, dtype=torch.float32, device=self.device)
+        self.next_tok = torch.empty(batch, dtype=torch.int32, device=self.device)
+        need = max(256, lib().wh_decode_step_workspace(ctypes.byref(self.c_cfg), batch))
+        self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+
+    def wh_decode_step(self, tok, pos, cross_kv, n_ctx: int, stream=None):
+        """tok, pos: int32 device tensors [batch]; cross_kv: bf16 [n_layer][batch * n_ctx][2 d]
+        (wh_prepare_cross's output).  Returns (logits [batch][n_vocab], next_tok [batch])."""
+        import torch
+        assert tok.dtype == torch.int32 and pos.dtype == torch.int32 and cross_kv.dtype == torch.bfloat16
+        rc = lib().wh_decode_step(_ptr(tok), _ptr(pos), self.batch, ctypes.byref(self.c_cfg), ctypes.byref(self.c_w),
+                                  _ptr(self.kcache), _ptr(self.vcache), _ptr(cross_kv), n_ctx, _ptr(self.logits),
+                                  _ptr(self.next_tok), _ptr(self.workspace), self.workspace.numel(), _stream(stream))
+        _check(rc, "wh_decode_step")
+        return self.logits, self.next_tok
