@@ -269,6 +269,67 @@ def _encoder_flops(cfg, n_ctx):
     return stem + cfg.n_layer * block
 
 
+def _decoder_weights_on_device(cfg, seed=17):
+    """Random decoder weights of the workload's shape, drawn on the device (timing only):
+    matrices N(0, 0.02) bf16, biases N(0, 0.01), LayerNorm gamma 1 and beta 0."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    d, f, V = cfg.d_model, cfg.d_ff, cfg.n_vocab
+    mat = lambda r, c: (0.02 * torch.randn(r, c, device="cuda", generator=g)).to(torch.bfloat16)
+    vec = lambda n, std=0.01: std * torch.randn(n, device="cuda", generator=g)
+    one, zero = torch.ones(d, device="cuda"), torch.zeros(d, device="cuda")
+    layers = []
+    for _ in range(cfg.n_layer):
+        lw = {k: mat(d, d) for k in ("wq", "wk", "wv", "wo", "xwq", "xwo")}
+        lw.update(w1=mat(f, d), w2=mat(d, f), b1=vec(f))
+        lw.update({k: vec(d) for k in ("bq", "bv", "bo", "xbq", "xbo", "b2")})
+        lw.update(ln1_g=one, ln1_b=zero, lnx_g=one, lnx_b=zero, ln2_g=one, ln2_b=zero)
+        layers.append(lw)
+    return {"tok_embd": mat(V, d), "dec_pos": 0.02 * torch.randn(448, d, device="cuda", generator=g),
+            "layers": layers, "lnf_g": one, "lnf_b": zero}
+
+
+def _time_decode(cfg, B, kv, steps, timed):
+    """One decoder step of the workload's decoder (as many layers as the encoder, its width,
+    vocabulary cfg.n_vocab, 448 text positions) for B sequences at position 224 (half the
+    text context), cross-attending over wh_prepare_cross's K/V of this batch's memory;
+    recorded once (wh_graph_capture_decode) and replayed.  Algorithmic bytes per step: every
+    decoder weight and the token embedding once, each sequence's cross K/V of every layer,
+    its self-attention cache rows 0..pos read and row pos written."""
+    import torch
+
+    from whisper_audio_encoder_gb300 import wh
+    d, f, L, V, pos = cfg.d_model, cfg.d_ff, cfg.n_layer, cfg.n_vocab, 224
+    dec = wh.Decoder(cfg.n_head, _decoder_weights_on_device(cfg), B)
+    tok = torch.randint(0, V, (B,), dtype=torch.int32, device="cuda")
+    posd = torch.full((B,), pos, dtype=torch.int32, device="cuda")
+    gs = torch.cuda.Stream()
+    graph = dec.capture(tok, posd, kv, 1500, gs)
+    with torch.cuda.stream(gs):
+        ms = timed(lambda: graph.launch(gs), max(20, steps))
+    # the same step called directly, per kernel class (events around every launch)
+    wh.wh_trace_enable(True)
+    ms_direct = timed(lambda: dec.wh_decode_step(tok, posd, kv, 1500), 10)
+    stats = wh.wh_trace_read()
+    wh.wh_trace_enable(False)
+    graph.destroy()
+    st = wh.wh_status()
+    if st != wh.WH_OK:
+        raise RuntimeError(f"device status after the decode step: {wh.wh_strerror(st)}")
+    wbytes = 2.0 * (L * (6.0 * d * d + 2.0 * d * f) + V * d)
+    kvbytes = 2.0 * L * B * (1500 * 2 * d + (pos + 1) * 2 * d + 2 * d)
+    nbytes = wbytes + kvbytes
+    peaks = _peaks()
+    calls = 11  # the timed() warm-up call plus 10
+    per = {k: [_r(v["total_ms"] / calls * 1e3, 1), _r(v["bytes"] / (v["total_ms"] * 1e-3) / 1e9, 0)]
+           for k, v in stats.items() if k in ("dec_gemm", "decode_attention", "dec_other")}
+    del dec
+    return {"us_per_step": _r(ms * 1e3, 1), "tokens_per_s": _r(B * 1000.0 / ms, 0),
+            "us_per_layer": _r(ms * 1e3 / max(1, L), 2), "gbs": _r(nbytes / (ms * 1e-3) / 1e9, 0),
+            "frac_hbm": _r(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4), "mb_per_step": _r(nbytes / 1e6, 1),
+            "direct_us": _r(ms_direct * 1e3, 1), "per_class_us_gbs": per}
+
+
 def _time_next(enc, cfg, B, pcm_d, mel_d, out_d, steps):
     import torch
 
@@ -294,6 +355,7 @@ def _time_next(enc, cfg, B, pcm_d, mel_d, out_d, steps):
     # wh_prepare_cross: K, V of every decoder layer from the batch's encoder memory
     res["cross_kv"] = {"ms_per_batch": _r(ms, 3), "tflops": _r(flops / (ms * 1e-3) / 1e12, 1),
                        "decoder_layers": ckv.n_layer}
+    res["decode_step"] = _time_decode(cfg, B, kv, steps, timed)
     del kv, ckv
     # one decoder step's cross-attention of one layer: one query per (window, head) over the
     # 1500 keys and values of that layer's [K | V] rows.  Calls cycle over 4 layers (4 x 123 MB

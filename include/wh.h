@@ -355,6 +355,15 @@ size_t wh_decode_step_workspace(const wh_dec_config *cfg, int batch);
 int wh_decode_step(const int *tok, const int *pos, int batch, const wh_dec_config *cfg, const wh_dec_weights *w,
                    wh_bf16 *kcache, wh_bf16 *vcache, const wh_bf16 *cross_kv, int n_ctx, float *logits,
                    int *next_tok, void *workspace, size_t ws_bytes, void *stream);
+/* One decoder step recorded into a CUDA graph (wh_decode_step's arguments; replay with
+ * wh_graph_launch, free with wh_graph_destroy; stream not NULL).  tok and pos are read from
+ * device memory at every replay, so a decode loop refreshes them in place (next_tok -> tok,
+ * pos + 1 -> pos) and replays; the caches, cross K/V, logits and workspace are the recorded
+ * buffers. */
+int wh_graph_capture_decode(const int *tok, const int *pos, int batch, const wh_dec_config *cfg,
+                            const wh_dec_weights *w, wh_bf16 *kcache, wh_bf16 *vcache, const wh_bf16 *cross_kv,
+                            int n_ctx, float *logits, int *next_tok, void *workspace, size_t ws_bytes, void *stream,
+                            wh_graph **graph);
 
 /* ---------------------------------------------------------------------------------------
  * Status, errors, tracing

@@ -179,3 +179,33 @@ def test_repeated_step_is_bitwise_identical():
     a, na, _ = c.step([1, 2, 3], [4, 9, 2])
     b, nb, _ = c.step([1, 2, 3], [4, 9, 2])           # rewrites the same cache rows
     assert np.array_equal(a, b) and np.array_equal(na, nb)
+
+
+def test_recorded_step_replays_the_direct_call_and_follows_new_tokens():
+    """wh_graph_capture_decode: a replay gives the direct call's logits bit for bit, and
+    reads tok / pos afresh at every replay (a decode loop refreshes them in place)."""
+    c = Case(TINY, n_layer=2, n_vocab=2000, cap=24, batch=3, n_ctx=37, seed=11)
+    c.prefill([3, 3, 3])
+    tok = torch.tensor([5, 6, 7], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([3, 3, 3], dtype=torch.int32, device="cuda")
+    k0, v0 = c.dec.kcache.clone(), c.dec.vcache.clone()
+    ref = [c.dec.wh_decode_step(tok, pos, c.kv_dev, c.n_ctx)[0].clone()]
+    tok2 = c.dec.next_tok.clone()
+    pos.add_(1)
+    ref.append(c.dec.wh_decode_step(tok2, pos, c.kv_dev, c.n_ctx)[0].clone())
+    c.dec.kcache.copy_(k0)
+    c.dec.vcache.copy_(v0)
+    pos.fill_(3)
+    s = torch.cuda.Stream()
+    graph = c.dec.capture(tok, pos, c.kv_dev, c.n_ctx, s)
+    graph.launch(s)
+    s.synchronize()
+    assert torch.equal(c.dec.logits, ref[0])
+    with torch.cuda.stream(s):
+        tok.copy_(c.dec.next_tok)
+        pos.add_(1)
+    graph.launch(s)
+    s.synchronize()
+    assert torch.equal(c.dec.logits, ref[1])
+    graph.destroy()
+    assert wh.wh_status() == wh.WH_OK

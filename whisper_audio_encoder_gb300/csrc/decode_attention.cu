@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(DA_THREADS) k_decode_attention(const DecAttnAr
     const int s = blockIdx.y, h = blockIdx.x, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane >> 2, sub = lane & 3;   // key slot in the warp, 16-dim quarter
+    pdl_launch_dependents();
+    pdl_wait();
     int nk = p.max_keys;
     if (p.n_keys) {   // a count outside 0 .. max_keys is clamped and reported as WH_EBOUNDS
         const int want = p.n_keys[b];
@@ -200,16 +202,23 @@ __global__ void __launch_bounds__(DA_THREADS) k_decode_attention(const DecAttnAr
 
 }  // namespace
 
-size_t decode_attention_workspace(int batch, int n_head, int max_keys) {
-    if (batch <= 0 || n_head <= 0 || max_keys <= 0) return 0;
+size_t decode_attention_ticket_offset(int batch, int n_head, int max_keys) {
     const size_t max_splits = (size_t)(max_keys + KEYS_PER_ITER - 1) / KEYS_PER_ITER;
     const size_t bh = (size_t)batch * n_head;
-    return ((bh * max_splits * PART * sizeof(float) + 255) & ~(size_t)255) + ((bh * sizeof(int) + 255) & ~(size_t)255);
+    return (bh * max_splits * PART * sizeof(float) + 255) & ~(size_t)255;
+}
+
+size_t decode_attention_ticket_bytes(int batch, int n_head) { return (size_t)batch * n_head * sizeof(int); }
+
+size_t decode_attention_workspace(int batch, int n_head, int max_keys) {
+    if (batch <= 0 || n_head <= 0 || max_keys <= 0) return 0;
+    return decode_attention_ticket_offset(batch, n_head, max_keys) +
+           ((decode_attention_ticket_bytes(batch, n_head) + 255) & ~(size_t)255);
 }
 
 int decode_attention_launch(const void *q, const void *k, const void *v, long long row_stride, long long seq_stride,
                             const int *n_keys, int max_keys, int batch, int n_head, void *out, void *workspace,
-                            const DevCtl &ctl, int num_sms, cudaStream_t s) {
+                            const DevCtl &ctl, int num_sms, cudaStream_t s, bool pdl, bool zero_tickets) {
     if (batch <= 0) return WH_OK;
     const long long bh = (long long)batch * n_head;
     // about BLOCKS_PER_SM blocks per SM in total, at least 64 keys per block, chunks a
@@ -222,7 +231,6 @@ int decode_attention_launch(const void *q, const void *k, const void *v, long lo
     chunk = (chunk + KEYS_PER_ITER - 1) / KEYS_PER_ITER * KEYS_PER_ITER;
     splits = (max_keys + chunk - 1) / chunk;
     if (splits > 65535 || n_head > 65535) return WH_EINVAL;
-    const size_t max_splits = (size_t)(max_keys + KEYS_PER_ITER - 1) / KEYS_PER_ITER;
     DecAttnArgs a;
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.k = static_cast<const __nv_bfloat16 *>(k);
@@ -238,12 +246,21 @@ int decode_attention_launch(const void *q, const void *k, const void *v, long lo
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.part = static_cast<float *>(workspace);
     a.ticket = reinterpret_cast<int *>(static_cast<uint8_t *>(workspace) +
-                                       ((bh * max_splits * PART * sizeof(float) + 255) & ~(size_t)255));
-    if (splits > 1 && cudaMemsetAsync(a.ticket, 0, bh * sizeof(int), s) != cudaSuccess) return WH_ECUDA;
-    const dim3 grid(n_head, (unsigned)splits, batch);
-    k_decode_attention<<<grid, DA_THREADS, 0, s>>>(a);
+                                       decode_attention_ticket_offset(batch, n_head, max_keys));
+    if (zero_tickets && splits > 1 && cudaMemsetAsync(a.ticket, 0, bh * sizeof(int), s) != cudaSuccess)
+        return WH_ECUDA;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(n_head, (unsigned)splits, batch);
+    lc.blockDim = dim3(DA_THREADS);
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&lc, k_decode_attention, a);
     count_launch();
-    return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
 }
 
 }  // namespace wh

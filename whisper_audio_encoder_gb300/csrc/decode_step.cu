@@ -17,9 +17,12 @@
 // the M operand: a CTA computes D[128 features][B tokens] = W[n0 .. n0+127][K] X[B][K]^T with
 // tcgen05.mma (M = 128, N = B rounded up to 16, K = 16), both operands K-major from a TMA ring,
 // the accumulator in TMEM (lane = feature, column = token).  K is split across CTAs so that
-// every SM streams weights; each split writes its partial tile and the last split of a tile
-// to finish (an atomic ticket, no block waits for another) adds the partials in split order
-// and applies the epilogue, so the result does not depend on timing.
+// every SM streams weights: the splits of a tile are one thread-block cluster, each CTA stages
+// its partial tile in shared memory, and after a cluster barrier each CTA adds the partials of
+// its slice of the tile in split order through distributed shared memory and applies the
+// epilogue -- no partial sums go through global memory, and the result does not depend on
+// timing.  Launched with programmatic stream serialization: the weight stream starts while
+// the previous kernel is still running; only the activations wait for it.
 #include "common.cuh"
 #include "internal.h"
 
@@ -31,7 +34,7 @@ constexpr int SK_THREADS = 192;   // warp 0 TMA, warp 1 TMEM + MMA, warps 2..5 e
 constexpr int SK_STAGES = 4;
 constexpr int SK_BK = 64;
 constexpr int SK_W_BYTES = 128 * SK_BK * 2;   // one k-block of 128 weight rows
-constexpr int SK_MAX_SPLITS = 16;
+constexpr int SK_MAX_SPLITS = 8;    // splits of one tile form a (portable) cluster
 constexpr int SK_MAX_B = 256;
 
 enum SkMode { SK_QKV = 0, SK_BF16 = 1, SK_GELU = 2, SK_RESID = 3, SK_LOGITS = 4 };
@@ -42,8 +45,6 @@ struct SkArgs {
     void *out[3];
     int cap;                    // SK_QKV: cache rows per sequence
     const int *pos;             // SK_QKV: cache row of each sequence (already in range)
-    float *part;                // [splits][B][N] partial sums (gridDim.y > 1)
-    int *ticket;                // [tiles], zero on entry and on exit
     unsigned long long *amax;   // SK_LOGITS: per-sequence (logit key, ~index), zero on entry
     DevCtl ctl;
 };
@@ -66,7 +67,7 @@ __device__ __forceinline__ void sk_finish(const SkArgs &p, int b, int n, float b
     v += bias;
     if constexpr (MODE == SK_QKV) {
         const int seg = n / p.seg_n, nin = n - seg * p.seg_n;
-        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out[seg]);
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(seg == 0 ? p.out[0] : (seg == 1 ? p.out[1] : p.out[2]));
         const long long row = seg == 0 ? b : (long long)b * p.cap + __ldg(p.pos + b);
         o[row * p.seg_n + nin] = __float2bfloat16_rn(v);
     } else if constexpr (MODE == SK_BF16 || MODE == SK_GELU) {
@@ -107,13 +108,14 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
     uint64_t *drain = accf + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    __shared__ int last_split, epi_fail;
+    __shared__ int epi_fail;
     __shared__ unsigned long long cta_best[SK_MAX_B];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, splits = gridDim.y;
     const int n0 = tile * 128, seg = n0 / p.seg_n, nin0 = n0 - seg * p.seg_n;
     const int kb0 = split * p.kb_per, kb1 = min(p.num_kb, kb0 + p.kb_per);
+    const CUtensorMap *wmap = seg == 0 ? &tw.w[0] : (seg == 1 ? &tw.w[1] : &tw.w[2]);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < SK_STAGES; ++s) {
@@ -125,13 +127,14 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
         *abort_flag = 0;
         epi_fail = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tw.w[seg]);
+        tma_prefetch_desc(wmap);
         tma_prefetch_desc(&tx);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
         tmem_relinquish();
     }
+    pdl_launch_dependents();   // the next kernel may start its own weight stream now
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -139,16 +142,26 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
-        int stage = 0;
-        uint32_t phase = 0, issued = 0, last_parity = 0;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        // The weights do not depend on earlier kernels: the first ring's worth is requested
+        // before waiting for the previous kernel, whose output (the activations x) follows.
+        const int pre = kb1 - kb0 < SK_STAGES ? kb1 - kb0 : SK_STAGES;
+        for (int i = 0; i < pre; ++i) {
+            mbar_arrive_expect_tx(full + i, (uint32_t)(SK_W_BYTES + p.x_bytes));
+            tma_load_2d(smem + i * p.stage_bytes, wmap, full + i, (kb0 + i) * SK_BK, nin0);
+        }
+        pdl_wait();
+        for (int i = 0; i < pre; ++i)
+            tma_load_2d(smem + i * p.stage_bytes + SK_W_BYTES, &tx, full + i, (kb0 + i) * SK_BK, 0);
+        int stage = pre % SK_STAGES;
+        uint32_t phase = pre == SK_STAGES ? 1u : 0u, issued = (1u << pre) - 1u, last_parity = 0;
+        for (int kb = kb0 + pre; kb < kb1; ++kb) {
             if (*abort_flag || !mbar_wait(empty + stage, phase ^ 1u, p.ctl)) {
                 *abort_flag = 1;
                 break;
             }
             uint8_t *sw = smem + stage * p.stage_bytes;
             mbar_arrive_expect_tx(full + stage, (uint32_t)(SK_W_BYTES + p.x_bytes));
-            tma_load_2d(sw, &tw.w[seg], full + stage, kb * SK_BK, nin0);
+            tma_load_2d(sw, wmap, full + stage, kb * SK_BK, nin0);
             tma_load_2d(sw + SK_W_BYTES, &tx, full + stage, kb * SK_BK, 0);
             issued |= 1u << stage;
             last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -192,9 +205,9 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
         const int q = warp & 3, n = n0 + 32 * q + lane;
         if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(accf, 0, p.ctl)) && lane == 0) epi_fail = 1;
         float bias = 0.0f;
-        if (MODE != SK_LOGITS) {
+        if (MODE != SK_LOGITS && splits == 1) {
             const int sg = n / p.seg_n;
-            const float *bp = p.bias[sg];
+            const float *bp = sg == 0 ? p.bias[0] : (sg == 1 ? p.bias[1] : p.bias[2]);
             if (bp != nullptr) bias = __ldg(bp + (n - sg * p.seg_n));
         }
         if (MODE == SK_LOGITS)
@@ -203,9 +216,11 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
         // one verdict for all four epilogue warps, so that they all reach the same barriers
         const bool ok = epi_fail == 0;
         if (!ok) *abort_flag = 1;
+        pdl_wait();   // earlier kernels' outputs (x, the cache rows) are complete and visible
         if (ok) {
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16);
+            float *P = reinterpret_cast<float *>(smem);   // the ring is free once the MMAs are done
             for (int c = 0; c < p.B_pad; c += 16) {
                 uint32_t r[16];
                 tmem_ld16(tbase + (uint32_t)c, r);
@@ -216,7 +231,7 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
                     if (b >= p.B) break;
                     const float v = __uint_as_float(r[j]);
                     if (splits > 1) {
-                        if (n < p.N) __stcg(p.part + ((long long)split * p.B + b) * p.N + n, v);
+                        P[b * 128 + 32 * q + lane] = v;   // this split's partial, [token][feature]
                     } else {
                         unsigned long long best = 0ull;
                         sk_finish<MODE>(p, b, n, bias, v, best);
@@ -228,29 +243,6 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
                 }
             }
         }
-        tc_fence_before();
-        if (ok && splits > 1) {
-            // the last split of this tile to finish adds the partials in split order
-            __threadfence();
-            epi_bar();
-            if (threadIdx.x == 64) last_split = atomicAdd(p.ticket + tile, 1) == splits - 1;
-            epi_bar();
-            if (last_split) {
-                __threadfence();
-                for (int b = 0; b < p.B; ++b) {
-                    float v = 0.0f;
-                    if (n < p.N)
-                        for (int s = 0; s < splits; ++s) v += __ldcg(p.part + ((long long)s * p.B + b) * p.N + n);
-                    unsigned long long best = 0ull;
-                    if (n < p.N || MODE == SK_LOGITS) sk_finish<MODE>(p, b, n, bias, v, best);
-                    if constexpr (MODE == SK_LOGITS) {
-                        best = warp_max_u64(best);
-                        if (lane == 0) atomicMax(cta_best + b, best);
-                    }
-                }
-                if (threadIdx.x == 64) p.ticket[tile] = 0;   // ready for the next launch
-            }
-        }
         if (MODE == SK_LOGITS) {
             epi_bar();
             for (int b = threadIdx.x - 64; b < p.B; b += 128)
@@ -258,6 +250,41 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
         }
     }
     tc_fence_before();
+    if (MODE != SK_LOGITS && splits > 1) {
+        // The splits of this tile are one cluster.  Once every CTA's partial is in its shared
+        // memory, CTA r adds, for its slice of the tile's features, the partials of all splits
+        // in split order (read through distributed shared memory) and finishes them.  Every
+        // thread of every CTA of the cluster reaches both cluster barriers on every path.
+        cluster_sync();
+        pdl_wait();
+        if (!*abort_flag) {
+            const int per = (128 + splits - 1) / splits, f0 = split * per;
+            const int len = min(128, f0 + per) - f0;
+            const uint32_t pl = smem_u32(smem);
+            uint32_t peer[SK_MAX_SPLITS];
+#pragma unroll
+            for (int r = 0; r < SK_MAX_SPLITS; ++r) peer[r] = r < splits ? mapa_shared(smem, (uint32_t)r) : pl;
+            for (int i = threadIdx.x; i < len * p.B; i += SK_THREADS) {
+                const int b = i / len, nl = f0 + (i - b * len), nn = n0 + nl;
+                const uint32_t off = (uint32_t)(b * 128 + nl) * 4u;
+                float pv[SK_MAX_SPLITS];
+#pragma unroll
+                for (int r = 0; r < SK_MAX_SPLITS; ++r) {
+                    pv[r] = 0.0f;
+                    if (r < splits) asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(pv[r]) : "r"(peer[r] + off));
+                }
+                float v = 0.0f;
+#pragma unroll
+                for (int r = 0; r < SK_MAX_SPLITS; ++r)
+                    if (r < splits) v += pv[r];
+                const int sg = nn / p.seg_n;
+                const float *bp = sg == 0 ? p.bias[0] : (sg == 1 ? p.bias[1] : p.bias[2]);
+                unsigned long long best = 0ull;
+                sk_finish<MODE>(p, b, nn, bp != nullptr ? __ldg(bp + (nn - sg * p.seg_n)) : 0.0f, v, best);
+            }
+        }
+        cluster_sync();   // no CTA leaves while a peer may still read its partial
+    }
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -326,13 +353,11 @@ int dec_gemm_prepare() {
            sk_set_attr<SK_LOGITS>();
 }
 
-size_t dec_gemm_partials(int batch, int n_max) { return (size_t)SK_MAX_SPLITS * batch * n_max * sizeof(float); }
-
 // y = epilogue(x[batch][K] w[N][K]^T + bias) for one of the SkMode epilogues.  w may be up to
 // three segments of seg_n rows (QKV); N = segments x seg_n, or any N for the logits.
 int dec_gemm_launch(int mode, const void *x, int batch, int K, const void *const w[3], int seg_n, int N,
-                    const float *const bias[3], void *const out[3], int cap, const int *pos, float *part,
-                    int *ticket, unsigned long long *amax, const DevCtl &ctl, int num_sms, cudaStream_t s) {
+                    const float *const bias[3], void *const out[3], int cap, const int *pos,
+                    unsigned long long *amax, const DevCtl &ctl, int num_sms, cudaStream_t s) {
     if (batch < 1 || batch > SK_MAX_B || K < 8 || K % 8 != 0 || N < 1 || seg_n < 1) return WH_EINVAL;
     if (mode != SK_LOGITS && (seg_n % 128 != 0 || N % seg_n != 0 || N / seg_n > 3)) return WH_EINVAL;
     const int b_pad = sk_b_pad(batch);
@@ -351,8 +376,6 @@ int dec_gemm_launch(int mode, const void *x, int batch, int K, const void *const
     }
     a.cap = cap;
     a.pos = pos;
-    a.part = part;
-    a.ticket = ticket;
     a.amax = amax;
     a.ctl = ctl;
     SkMaps tw;
@@ -362,25 +385,33 @@ int dec_gemm_launch(int mode, const void *x, int batch, int K, const void *const
     CUtensorMap tx;
     if (int rc = make_tmap_bf16(&tx, x, batch, K, K, b_pad)) return rc;
     const int tiles = (N + 127) / 128;
-    // split K so that about two CTAs per SM stream weights; every split gets >= 1 k-block
+    // split K so that about one CTA per SM streams weights; the splits of a tile form a
+    // cluster of at most SK_MAX_SPLITS CTAs, and every split gets >= 1 k-block
     int splits = 1;
     if (mode != SK_LOGITS) {
-        const int target = 2 * num_sms;
-        splits = (target + tiles - 1) / tiles;
+        splits = (num_sms + tiles / 2) / tiles;
         splits = splits < 1 ? 1 : (splits > SK_MAX_SPLITS ? SK_MAX_SPLITS : splits);
         splits = splits > a.num_kb ? a.num_kb : splits;
     }
     a.kb_per = (a.num_kb + splits - 1) / splits;
     splits = (a.num_kb + a.kb_per - 1) / a.kb_per;
-    if (tiles > 65535 * 16) return WH_EINVAL;
-    const dim3 grid(tiles, splits);
+    if (tiles > 2147483647 / 128) return WH_EINVAL;
     const int smem = sk_smem_bytes(b_pad);
     cudaError_t e;
     cudaLaunchConfig_t lc = {};
-    lc.gridDim = grid;
+    lc.gridDim = dim3(tiles, splits);
     lc.blockDim = dim3(SK_THREADS);
     lc.dynamicSmemBytes = smem;
     lc.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = splits;
+    attr[1].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = splits > 1 ? 2 : 1;
     switch (mode) {
         case SK_QKV: e = cudaLaunchKernelEx(&lc, k_dec_gemm<SK_QKV>, tw, tx, a); break;
         case SK_BF16: e = cudaLaunchKernelEx(&lc, k_dec_gemm<SK_BF16>, tw, tx, a); break;
@@ -421,14 +452,11 @@ constexpr int DEC_MAX_CROSS = 1500;   // encoder positions
 size_t up256d(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct DecLayout {
-    size_t x, xn, q, ao, h, pos_c, n_self, amax, part, ticket, da, total;
-    size_t ticket_bytes;
+    size_t x, xn, q, ao, h, pos_c, n_self, amax, da_self, da_cross, total;
 };
 
 DecLayout dec_layout(const wh_dec_config *c, int batch) {
     const size_t B = batch, d = c->d_model, f = c->d_ff;
-    const int n_max = 3 * c->d_model > c->d_ff ? 3 * c->d_model : c->d_ff;
-    const int keys = c->n_text_ctx > DEC_MAX_CROSS ? c->n_text_ctx : DEC_MAX_CROSS;
     DecLayout L;
     size_t off = 0;
     L.x = off;      off += up256d(B * d * 4);
@@ -439,10 +467,10 @@ DecLayout dec_layout(const wh_dec_config *c, int batch) {
     L.pos_c = off;  off += up256d(B * 4);
     L.n_self = off; off += up256d(B * 4);
     L.amax = off;   off += up256d(B * 8);
-    L.part = off;   off += up256d(dec_gemm_partials(batch, n_max));
-    L.ticket_bytes = (size_t)((n_max + 127) / 128) * 4;
-    L.ticket = off; off += up256d(L.ticket_bytes);
-    L.da = off;     off += up256d(decode_attention_workspace(batch, c->n_head, keys));
+    // one region each for the self- and the cross-attention, so that each keeps its merge
+    // tickets zero between calls
+    L.da_self = off;  off += up256d(decode_attention_workspace(batch, c->n_head, c->n_text_ctx));
+    L.da_cross = off; off += up256d(decode_attention_workspace(batch, c->n_head, DEC_MAX_CROSS));
     L.total = off;
     return L;
 }
@@ -505,15 +533,17 @@ extern "C" int wh_decode_step(const int *tok, const int *pos, int batch, const w
     void *xn = ws + L.xn, *q = ws + L.q, *ao = ws + L.ao, *hb = ws + L.h;
     int *pos_c = reinterpret_cast<int *>(ws + L.pos_c), *n_self = reinterpret_cast<int *>(ws + L.n_self);
     unsigned long long *amax = reinterpret_cast<unsigned long long *>(ws + L.amax);
-    float *part = reinterpret_cast<float *>(ws + L.part);
-    int *ticket = reinterpret_cast<int *>(ws + L.ticket);
-    void *da = ws + L.da;
+    uint8_t *da_self = ws + L.da_self, *da_cross = ws + L.da_cross;
     const size_t layer_cache = (size_t)batch * cap * d;
     const size_t layer_cross = (size_t)batch * n_ctx * 2 * d;
     int rc;
 
     trace_begin(TR_DEC_OTHER, s);
-    if (cudaMemsetAsync(ticket, 0, L.ticket_bytes, s) != cudaSuccess) return WH_ECUDA;
+    // every merge ticket of the step starts at zero (each launch leaves its own at zero)
+    const size_t da_tickets = decode_attention_ticket_bytes(batch, H);
+    if (cudaMemsetAsync(da_self + decode_attention_ticket_offset(batch, H, cap), 0, da_tickets, s) != cudaSuccess ||
+        cudaMemsetAsync(da_cross + decode_attention_ticket_offset(batch, H, n_ctx), 0, da_tickets, s) != cudaSuccess)
+        return WH_ECUDA;
     rc = dec_embed_launch(tok, pos, w->tok_embd, w->pos, d, V, cap, batch, x, pos_c, n_self, amax, ctl, s);
     trace_end(TR_DEC_OTHER, s, 0.0, (double)batch * d * 10.0);
     if (rc) return rc;
@@ -524,22 +554,22 @@ extern "C" int wh_decode_step(const int *tok, const int *pos, int batch, const w
         const float *bv[3] = {b0, b1, b2};
         void *ov[3] = {o0, o1, o2};
         trace_begin(TR_DEC_GEMM, s);
-        const int r = dec_gemm_launch(mode, a, batch, K, wv, seg_n, N, bv, ov, cap, pos_c, part, ticket, amax, ctl,
+        const int r = dec_gemm_launch(mode, a, batch, K, wv, seg_n, N, bv, ov, cap, pos_c, amax, ctl,
                                       num_sms, s);
         trace_end(TR_DEC_GEMM, s, 2.0 * batch * (double)N * K, 2.0 * (double)N * K + 2.0 * batch * (double)K);
         return r;
     };
     auto ln = [&](const float *g, const float *b) {
         trace_begin(TR_DEC_OTHER, s);
-        const int r = layernorm_launch(x, batch, d, g, b, xn, 1, s);
+        const int r = layernorm_launch(x, batch, d, g, b, xn, 1, s, true);
         trace_end(TR_DEC_OTHER, s, 0.0, (double)batch * d * 6.0);
         return r;
     };
     auto attend = [&](const void *qp, const void *kp, const void *vp, long long row_stride, long long seq_stride,
-                      const int *nk, int max_keys) {
+                      const int *nk, int max_keys, void *da) {
         trace_begin(TR_DEC_ATTN, s);
         const int r = decode_attention_launch(qp, kp, vp, row_stride, seq_stride, nk, max_keys, batch, H, ao, da, ctl,
-                                              num_sms, s);
+                                              num_sms, s, true, false);
         trace_end(TR_DEC_ATTN, s, 4.0 * batch * (double)max_keys * d, 4.0 * batch * (double)max_keys * d);
         return r;
     };
@@ -552,14 +582,14 @@ extern "C" int wh_decode_step(const int *tok, const int *pos, int batch, const w
         // query attends over rows 0 .. pos
         if ((rc = ln(Lw.ln1_g, Lw.ln1_b))) return rc;
         if ((rc = gemm(SK_QKV, xn, d, Lw.wq, Lw.wk, Lw.wv, d, 3 * d, Lw.bq, nullptr, Lw.bv, q, kc, vc))) return rc;
-        if ((rc = attend(q, kc, vc, d, (long long)cap * d, n_self, cap))) return rc;
+        if ((rc = attend(q, kc, vc, d, (long long)cap * d, n_self, cap, da_self))) return rc;
         if ((rc = gemm(SK_RESID, ao, d, Lw.wo, nullptr, nullptr, d, d, Lw.bo, nullptr, nullptr, x, nullptr, nullptr)))
             return rc;
         // cross-attention into the encoder memory (keys / values cached once per clip)
         if ((rc = ln(Lw.lnx_g, Lw.lnx_b))) return rc;
         if ((rc = gemm(SK_BF16, xn, d, Lw.xwq, nullptr, nullptr, d, d, Lw.xbq, nullptr, nullptr, q, nullptr, nullptr)))
             return rc;
-        if ((rc = attend(q, ckv, ckv + d, 2LL * d, (long long)n_ctx * 2 * d, nullptr, n_ctx))) return rc;
+        if ((rc = attend(q, ckv, ckv + d, 2LL * d, (long long)n_ctx * 2 * d, nullptr, n_ctx, da_cross))) return rc;
         if ((rc = gemm(SK_RESID, ao, d, Lw.xwo, nullptr, nullptr, d, d, Lw.xbo, nullptr, nullptr, x, nullptr,
                        nullptr)))
             return rc;

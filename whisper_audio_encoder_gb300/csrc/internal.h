@@ -47,8 +47,10 @@ int frontend_launch(const float *pcm, int64_t n, int64_t stride, int64_t total, 
 int frontend_ctl(DevCtl *ctl, int *num_sms);   // the current device's control block and SM count
 
 // ---- other kernels ---------------------------------------------------------------------
+// pdl: launched with programmatic stream serialization (may start before the previous kernel
+// has finished; waits for it before reading x)
 int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,
-                     cudaStream_t s);
+                     cudaStream_t s, bool pdl = false);
 int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
                      int num_sms, cudaStream_t s);
 int attention_prepare();
@@ -62,9 +64,15 @@ int resample_prepare();
 void resample_forget();   // drops the per-rate filter normalisers (wh_shutdown)
 // one-query attention of a decoder step, keys split across blocks (decode_attention.cu)
 size_t decode_attention_workspace(int batch, int n_head, int max_keys);
+// pdl: as for layernorm_launch.  zero_tickets = false: the caller guarantees that the merge
+// tickets in the workspace (at decode_attention_ticket_offset, decode_attention_ticket_bytes)
+// are zero, as every call leaves them.
 int decode_attention_launch(const void *q, const void *k, const void *v, long long row_stride, long long seq_stride,
                             const int *n_keys, int max_keys, int batch, int n_head, void *out, void *workspace,
-                            const DevCtl &ctl, int num_sms, cudaStream_t s);
+                            const DevCtl &ctl, int num_sms, cudaStream_t s, bool pdl = false,
+                            bool zero_tickets = true);
+size_t decode_attention_ticket_offset(int batch, int n_head, int max_keys);
+size_t decode_attention_ticket_bytes(int batch, int n_head);
 // conv1's im2col matrix over the first n_frames (<= 3000) frames of each window's log-mel
 int stem_im2col_launch(const float *mel, int batch, int n_mels, int n_frames, void *a1, cudaStream_t s);
 // y (bf16) = x (float32), n a multiple of 4, both 16-byte aligned

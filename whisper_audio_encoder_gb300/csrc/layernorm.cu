@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restric
     constexpr int CAP = NV > 0 ? NV : MAXV;
     const int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();
     if (row >= rows) return;
     const int nv = NV > 0 ? NV : d >> 7;
     if (NV > 0) d = NV * 128;
@@ -67,13 +69,27 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restric
         }
 }
 
+// Launch configuration; with pdl the kernel may start while the previous kernel of the stream
+// is still running (it waits for that kernel's results before reading x).
+cudaLaunchConfig_t ln_config(int grid, cudaStream_t s, bool pdl, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3(LN_THREADS);
+    lc.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = pdl ? 1 : 0;
+    return lc;
+}
+
 template <int NV>
-void launch_ln(int grid, cudaStream_t s, const float *x, int rows, int d, const float *g, const float *b, void *y,
-               int y_bf16) {
-    if (y_bf16)
-        k_layernorm<NV, true><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
-    else
-        k_layernorm<NV, false><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+cudaError_t launch_ln(int grid, cudaStream_t s, bool pdl, const float *x, int rows, int d, const float *g,
+                      const float *b, void *y, int y_bf16) {
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t lc = ln_config(grid, s, pdl, attr);
+    return y_bf16 ? cudaLaunchKernelEx(&lc, k_layernorm<NV, true>, x, rows, d, g, b, y)
+                  : cudaLaunchKernelEx(&lc, k_layernorm<NV, false>, x, rows, d, g, b, y);
 }
 
 // d a multiple of 64 but not of 128: float2 per lane.
@@ -83,6 +99,8 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm64(const float *__restr
                                                             const float *__restrict__ b, void *__restrict__ y) {
     const int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();
     if (row >= rows) return;
     const int nv = d >> 6;
     const float2 *xr = reinterpret_cast<const float2 *>(x + (long long)row * d);
@@ -123,27 +141,28 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm64(const float *__restr
 }  // namespace
 
 int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,
-                     cudaStream_t s) {
+                     cudaStream_t s, bool pdl) {
     if (rows <= 0) return WH_OK;
     if (d % 64 != 0 || d < 64 || d > 128 * MAXV) return WH_EINVAL;
     const int grid = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
+    cudaError_t e;
     if (d % 128 == 0) {
         switch (d / 128) {  // the family's widths (384, 512, 768, 1024, 1280) get exact registers
-            case 3: launch_ln<3>(grid, s, x, rows, d, g, b, y, y_bf16); break;
-            case 4: launch_ln<4>(grid, s, x, rows, d, g, b, y, y_bf16); break;
-            case 6: launch_ln<6>(grid, s, x, rows, d, g, b, y, y_bf16); break;
-            case 8: launch_ln<8>(grid, s, x, rows, d, g, b, y, y_bf16); break;
-            case 10: launch_ln<10>(grid, s, x, rows, d, g, b, y, y_bf16); break;
-            default: launch_ln<0>(grid, s, x, rows, d, g, b, y, y_bf16); break;
+            case 3: e = launch_ln<3>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
+            case 4: e = launch_ln<4>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
+            case 6: e = launch_ln<6>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
+            case 8: e = launch_ln<8>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
+            case 10: e = launch_ln<10>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
+            default: e = launch_ln<0>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
         }
     } else {
-        if (y_bf16)
-            k_layernorm64<true><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
-        else
-            k_layernorm64<false><<<grid, LN_THREADS, 0, s>>>(x, rows, d, g, b, y);
+        cudaLaunchAttribute attr[1];
+        const cudaLaunchConfig_t lc = ln_config(grid, s, pdl, attr);
+        e = y_bf16 ? cudaLaunchKernelEx(&lc, k_layernorm64<true>, x, rows, d, g, b, y)
+                   : cudaLaunchKernelEx(&lc, k_layernorm64<false>, x, rows, d, g, b, y);
     }
     count_launch();
-    return cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;
 }
 
 }  // namespace wh

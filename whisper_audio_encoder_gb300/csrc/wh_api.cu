@@ -603,6 +603,20 @@ int wh_graph_capture_encode(const float *mel, int batch, const wh_config *cfg, c
                         [&]() { return wh_encode(mel, batch, cfg, w, out, enc_ws, enc_ws_bytes, stream); });
 }
 
+int wh_graph_capture_decode(const int *tok, const int *pos, int batch, const wh_dec_config *cfg,
+                            const wh_dec_weights *w, wh_bf16 *kcache, wh_bf16 *vcache, const wh_bf16 *cross_kv,
+                            int n_ctx, float *logits, int *next_tok, void *workspace, size_t ws_bytes, void *stream,
+                            wh_graph **graph) {
+    if (!graph || !stream || batch <= 0) return WH_EINVAL;
+    *graph = nullptr;
+    DevState *st;
+    if (int rc = ensure_device(&st)) return rc;
+    return record_graph(static_cast<cudaStream_t>(stream), graph, [&]() {
+        return wh_decode_step(tok, pos, batch, cfg, w, kcache, vcache, cross_kv, n_ctx, logits, next_tok, workspace,
+                              ws_bytes, stream);
+    });
+}
+
 int wh_graph_launch(wh_graph *graph, void *stream) {
     if (!graph) return WH_EINVAL;
     count_launch();

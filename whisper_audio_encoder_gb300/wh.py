@@ -121,6 +121,9 @@ def lib():
         "wh_graph_capture_encode": (ctypes.c_int, [_p, ctypes.c_int, ctypes.POINTER(wh_config),
                                                    ctypes.POINTER(wh_weights), _p, _p, ctypes.c_size_t, _p,
                                                    ctypes.POINTER(ctypes.c_void_p)]),
+        "wh_graph_capture_decode": (ctypes.c_int, [_p, _p, ctypes.c_int, ctypes.POINTER(wh_dec_config),
+                                                   ctypes.POINTER(wh_dec_weights), _p, _p, _p, ctypes.c_int, _p, _p,
+                                                   _p, ctypes.c_size_t, _p, ctypes.POINTER(ctypes.c_void_p)]),
         "wh_graph_launch": (ctypes.c_int, [_p, _p]),
         "wh_graph_destroy": (ctypes.c_int, [_p]),
     }
@@ -539,7 +542,10 @@ class Decoder:
         self._keep = []
 
         def put(a, dtype):
-            t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dtype).to(self.device)
+            if isinstance(a, torch.Tensor):
+                t = a.to(device=self.device, dtype=dtype).contiguous()
+            else:
+                t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dtype).to(self.device)
             self._keep.append(t)
             return t.data_ptr()
 
@@ -576,3 +582,15 @@ class Decoder:
                                   _ptr(self.next_tok), _ptr(self.workspace), self.workspace.numel(), _stream(stream))
         _check(rc, "wh_decode_step")
         return self.logits, self.next_tok
+
+    def capture(self, tok, pos, cross_kv, n_ctx: int, stream):
+        """Records one wh_decode_step over these buffers (wh_graph_capture_decode); replay with
+        Graph.launch() after refreshing tok / pos in place."""
+        h = ctypes.c_void_p()
+        rc = lib().wh_graph_capture_decode(_ptr(tok), _ptr(pos), self.batch, ctypes.byref(self.c_cfg),
+                                           ctypes.byref(self.c_w), _ptr(self.kcache), _ptr(self.vcache),
+                                           _ptr(cross_kv), n_ctx, _ptr(self.logits), _ptr(self.next_tok),
+                                           _ptr(self.workspace), self.workspace.numel(), _stream(stream),
+                                           ctypes.byref(h))
+        _check(rc, "wh_graph_capture_decode")
+        return Graph(h, (tok, pos, cross_kv))
