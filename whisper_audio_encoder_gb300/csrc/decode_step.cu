@@ -41,6 +41,10 @@ enum SkMode { SK_QKV = 0, SK_BF16 = 1, SK_GELU = 2, SK_RESID = 3, SK_LOGITS = 4 
 
 struct SkArgs {
     int N, seg_n, num_kb, kb_per, B, B_pad, x_bytes, stage_bytes, tmem_cols;
+    // LayerNorm fused in front (xf != nullptr): the operand X is LN(xf) over K = d columns,
+    // built by the epilogue warps in shared memory at x_off instead of loaded by TMA
+    const float *xf, *ln_g, *ln_b;
+    int K, x_off, bar_off;
     const float *bias[3];
     void *out[3];
     int cap;                    // SK_QKV: cache rows per sequence
@@ -102,11 +106,12 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + SK_STAGES * p.stage_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
     uint64_t *empty = full + SK_STAGES;
     uint64_t *accf = empty + SK_STAGES;
     uint64_t *drain = accf + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *x_ready = drain + 1;      // LN-fused operand written (4 epilogue warps)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(x_ready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ int epi_fail;
     __shared__ unsigned long long cta_best[SK_MAX_B];
@@ -124,6 +129,7 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
         }
         mbar_init(accf, 1);
         mbar_init(drain, 1);
+        mbar_init(x_ready, 4);
         *abort_flag = 0;
         epi_fail = 0;
         fence_mbar_init();
@@ -150,8 +156,9 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
             tma_load_2d(smem + i * p.stage_bytes, wmap, full + i, (kb0 + i) * SK_BK, nin0);
         }
         pdl_wait();
-        for (int i = 0; i < pre; ++i)
-            tma_load_2d(smem + i * p.stage_bytes + SK_W_BYTES, &tx, full + i, (kb0 + i) * SK_BK, 0);
+        if (p.xf == nullptr)
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(smem + i * p.stage_bytes + SK_W_BYTES, &tx, full + i, (kb0 + i) * SK_BK, 0);
         int stage = pre % SK_STAGES;
         uint32_t phase = pre == SK_STAGES ? 1u : 0u, issued = (1u << pre) - 1u, last_parity = 0;
         for (int kb = kb0 + pre; kb < kb1; ++kb) {
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
             uint8_t *sw = smem + stage * p.stage_bytes;
             mbar_arrive_expect_tx(full + stage, (uint32_t)(SK_W_BYTES + p.x_bytes));
             tma_load_2d(sw, wmap, full + stage, kb * SK_BK, nin0);
-            tma_load_2d(sw + SK_W_BYTES, &tx, full + stage, kb * SK_BK, 0);
+            if (p.xf == nullptr) tma_load_2d(sw + SK_W_BYTES, &tx, full + stage, kb * SK_BK, 0);
             issued |= 1u << stage;
             last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == SK_STAGES) {
@@ -178,15 +185,17 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
         const uint32_t idesc = idesc_bf16_f32(128, p.B_pad);
         int stage = 0;
         uint32_t phase = 0;
-        bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        bool ok = p.xf == nullptr || (!*abort_flag && mbar_wait(x_ready, 0, p.ctl));
+        const uint32_t xr = smem_u32(smem + p.x_off);
+        for (int kb = kb0; ok && kb < kb1; ++kb) {
             if (*abort_flag || !mbar_wait(full + stage, phase, p.ctl)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + stage * p.stage_bytes);
-            const uint64_t ad = sdesc_sw128(sa), bd = sdesc_sw128(sa + SK_W_BYTES);
+            const uint64_t ad = sdesc_sw128(sa);
+            const uint64_t bd = sdesc_sw128(p.xf ? xr + (uint32_t)((kb - kb0) * p.B_pad * 128) : sa + SK_W_BYTES);
 #pragma unroll
             for (int k = 0; k < SK_BK / 16; ++k)
                 umma_bf16(tmem_base, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
@@ -203,6 +212,61 @@ __global__ void __launch_bounds__(SK_THREADS) k_dec_gemm(const __grid_constant__
     } else if (warp >= 2) {
         // ---------------- epilogue: feature n = n0 + 32 q + lane, every sequence ----------------
         const int q = warp & 3, n = n0 + 32 * q + lane;
+        if (p.xf != nullptr) {
+            // LayerNorm in front (eps 1e-5, biased variance): the epilogue warps write this
+            // split's k-blocks of bf16 LN(x) in the 128-byte-swizzled K-major layout the MMA
+            // reads; rows B .. B_pad-1 are zero.
+            pdl_wait();
+            const int kbs = kb1 - kb0, pad_rows = p.B_pad - p.B;
+            uint8_t *xs = smem + p.x_off;
+            for (int i = threadIdx.x - 64; i < kbs * pad_rows * 8; i += 128) {
+                const int kk = i / (pad_rows * 8), rem = i - kk * pad_rows * 8;
+                *reinterpret_cast<uint4 *>(xs + kk * p.B_pad * 128 + (p.B + (rem >> 3)) * 128 + (rem & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            // Each warp normalises rows b = w, w + 4, ...: the row in registers (16-byte loads),
+            // mean then centred variance, then this split's k-blocks written as bf16.
+            const int ew = warp - 2, nv = p.K >> 7;   // float4 per lane
+            for (int b = ew; b < p.B; b += 4) {
+                const float4 *xrow = reinterpret_cast<const float4 *>(p.xf + (long long)b * p.K);
+                float4 v[16];
+                float s0 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (i < nv) {
+                        v[i] = __ldcg(xrow + i * 32 + lane);
+                        s0 += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+                    }
+                const float mean = warp_sum(s0) / (float)p.K;
+                float q0 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (i < nv) {
+                        const float a = v[i].x - mean, c = v[i].y - mean, d2 = v[i].z - mean, e = v[i].w - mean;
+                        q0 = fmaf(a, a, fmaf(c, c, fmaf(d2, d2, fmaf(e, e, q0))));
+                    }
+                const float rstd = 1.0f / sqrtf(warp_sum(q0) / (float)p.K + 1e-5f);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (i < nv) {
+                        const int k = 4 * (i * 32 + lane), kb = k >> 6;
+                        if (kb >= kb0 && kb < kb1) {
+                            const float4 gg = __ldg(reinterpret_cast<const float4 *>(p.ln_g + k));
+                            const float4 bb = __ldg(reinterpret_cast<const float4 *>(p.ln_b + k));
+                            const uint2 w = make_uint2(pack_bf16((v[i].x - mean) * rstd * gg.x + bb.x,
+                                                                 (v[i].y - mean) * rstd * gg.y + bb.y),
+                                                       pack_bf16((v[i].z - mean) * rstd * gg.z + bb.z,
+                                                                 (v[i].w - mean) * rstd * gg.w + bb.w));
+                            const int ch = (k & 63) >> 3;
+                            *reinterpret_cast<uint2 *>(xs + (kb - kb0) * p.B_pad * 128 + b * 128 +
+                                                       ((ch ^ (b & 7)) << 4) + ((k & 7) >> 2) * 8) = w;
+                        }
+                    }
+            }
+            fence_proxy_async_smem();   // the tensor core reads what this warp wrote
+            __syncwarp();
+            if (lane == 0) mbar_arrive(x_ready);
+        }
         if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(accf, 0, p.ctl)) && lane == 0) epi_fail = 1;
         float bias = 0.0f;
         if (MODE != SK_LOGITS && splits == 1) {
@@ -355,9 +419,12 @@ int dec_gemm_prepare() {
 
 // y = epilogue(x[batch][K] w[N][K]^T + bias) for one of the SkMode epilogues.  w may be up to
 // three segments of seg_n rows (QKV); N = segments x seg_n, or any N for the logits.
-int dec_gemm_launch(int mode, const void *x, int batch, int K, const void *const w[3], int seg_n, int N,
-                    const float *const bias[3], void *const out[3], int cap, const int *pos,
-                    unsigned long long *amax, const DevCtl &ctl, int num_sms, cudaStream_t s) {
+// With xf given, X = LN(xf; ln_g, ln_b) is built inside the kernel (x is not read); if that
+// layout does not fit in shared memory, WH_ENOSPC is returned before anything is launched.
+int dec_gemm_launch(int mode, const void *x, const float *xf, const float *ln_g, const float *ln_b, int batch,
+                    int K, const void *const w[3], int seg_n, int N, const float *const bias[3], void *const out[3],
+                    int cap, const int *pos, unsigned long long *amax, const DevCtl &ctl, int num_sms,
+                    cudaStream_t s) {
     if (batch < 1 || batch > SK_MAX_B || K < 8 || K % 8 != 0 || N < 1 || seg_n < 1) return WH_EINVAL;
     if (mode != SK_LOGITS && (seg_n % 128 != 0 || N % seg_n != 0 || N / seg_n > 3)) return WH_EINVAL;
     const int b_pad = sk_b_pad(batch);
@@ -367,8 +434,14 @@ int dec_gemm_launch(int mode, const void *x, int batch, int K, const void *const
     a.num_kb = (K + SK_BK - 1) / SK_BK;
     a.B = batch;
     a.B_pad = b_pad;
-    a.x_bytes = b_pad * 128;
-    a.stage_bytes = sk_stage_bytes(b_pad);
+    const bool ln_in = xf != nullptr;
+    if (ln_in && (K % 128 != 0 || K > 2048)) return WH_EINVAL;
+    a.x_bytes = ln_in ? 0 : b_pad * 128;
+    a.stage_bytes = ln_in ? SK_W_BYTES : sk_stage_bytes(b_pad);
+    a.xf = xf;
+    a.ln_g = ln_g;
+    a.ln_b = ln_b;
+    a.K = K;
     a.tmem_cols = b_pad <= 32 ? 32 : (b_pad <= 64 ? 64 : (b_pad <= 128 ? 128 : 256));
     for (int i = 0; i < 3; ++i) {
         a.bias[i] = bias ? bias[i] : nullptr;
@@ -382,8 +455,9 @@ int dec_gemm_launch(int mode, const void *x, int batch, int K, const void *const
     const int nseg = mode == SK_LOGITS ? 1 : N / seg_n;
     for (int i = 0; i < 3; ++i)
         if (int rc = make_tmap_bf16(&tw.w[i], w[i < nseg ? i : 0], a.seg_n, K, K, 128)) return rc;
-    CUtensorMap tx;
-    if (int rc = make_tmap_bf16(&tx, x, batch, K, K, b_pad)) return rc;
+    CUtensorMap tx = tw.w[0];   // placeholder when the operand is built in the kernel
+    if (!ln_in)
+        if (int rc = make_tmap_bf16(&tx, x, batch, K, K, b_pad)) return rc;
     const int tiles = (N + 127) / 128;
     // split K so that about one CTA per SM streams weights; the splits of a tile form a
     // cluster of at most SK_MAX_SPLITS CTAs, and every split gets >= 1 k-block
@@ -396,7 +470,12 @@ int dec_gemm_launch(int mode, const void *x, int batch, int K, const void *const
     a.kb_per = (a.num_kb + splits - 1) / splits;
     splits = (a.num_kb + a.kb_per - 1) / a.kb_per;
     if (tiles > 2147483647 / 128) return WH_EINVAL;
-    const int smem = sk_smem_bytes(b_pad);
+    // shared memory: the weight ring (with the TMA-loaded X per stage unless LN is fused), the
+    // LN-built X of this split's k-blocks, the barriers, and slack for 1024-byte alignment
+    a.x_off = SK_STAGES * a.stage_bytes;
+    a.bar_off = a.x_off + (ln_in ? a.kb_per * b_pad * 128 : 0);
+    const int smem = a.bar_off + 128 + 1024;
+    if (smem > sk_smem_bytes(SK_MAX_B)) return WH_ENOSPC;
     cudaError_t e;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(tiles, splits);
@@ -548,21 +627,33 @@ extern "C" int wh_decode_step(const int *tok, const int *pos, int batch, const w
     trace_end(TR_DEC_OTHER, s, 0.0, (double)batch * d * 10.0);
     if (rc) return rc;
 
-    auto gemm = [&](int mode, const void *a, int K, const void *w0, const void *w1, const void *w2, int seg_n, int N,
-                    const float *b0, const float *b1, const float *b2, void *o0, void *o1, void *o2) {
+    // A dense layer; with g given, its input is LN(x; g, b), fused into the GEMM when the
+    // normalised operand fits in shared memory, else a LayerNorm launch writes xn first.
+    auto gemm = [&](int mode, const float *g, const float *b, const void *a, int K, const void *w0, const void *w1,
+                    const void *w2, int seg_n, int N, const float *b0, const float *b1, const float *b2, void *o0,
+                    void *o1, void *o2) {
         const void *wv[3] = {w0, w1 ? w1 : w0, w2 ? w2 : w0};
         const float *bv[3] = {b0, b1, b2};
         void *ov[3] = {o0, o1, o2};
+        int r = WH_ENOSPC;
         trace_begin(TR_DEC_GEMM, s);
-        const int r = dec_gemm_launch(mode, a, batch, K, wv, seg_n, N, bv, ov, cap, pos_c, amax, ctl,
-                                      num_sms, s);
+        if (g != nullptr)
+            r = dec_gemm_launch(mode, nullptr, x, g, b, batch, K, wv, seg_n, N, bv, ov, cap, pos_c, amax, ctl,
+                                num_sms, s);
+        trace_end(TR_DEC_GEMM, s, 2.0 * batch * (double)N * K,
+                  2.0 * (double)N * K + (g != nullptr ? 4.0 : 2.0) * batch * (double)K);
+        if (r != WH_ENOSPC) return r;
+        if (g != nullptr) {
+            trace_begin(TR_DEC_OTHER, s);
+            r = layernorm_launch(x, batch, d, g, b, xn, 1, s, true);
+            trace_end(TR_DEC_OTHER, s, 0.0, (double)batch * d * 6.0);
+            if (r) return r;
+            a = xn;
+        }
+        trace_begin(TR_DEC_GEMM, s);
+        r = dec_gemm_launch(mode, a, nullptr, nullptr, nullptr, batch, K, wv, seg_n, N, bv, ov, cap, pos_c, amax, ctl,
+                            num_sms, s);
         trace_end(TR_DEC_GEMM, s, 2.0 * batch * (double)N * K, 2.0 * (double)N * K + 2.0 * batch * (double)K);
-        return r;
-    };
-    auto ln = [&](const float *g, const float *b) {
-        trace_begin(TR_DEC_OTHER, s);
-        const int r = layernorm_launch(x, batch, d, g, b, xn, 1, s, true);
-        trace_end(TR_DEC_OTHER, s, 0.0, (double)batch * d * 6.0);
         return r;
     };
     auto attend = [&](const void *qp, const void *kp, const void *vp, long long row_stride, long long seq_stride,
@@ -580,30 +671,32 @@ extern "C" int wh_decode_step(const int *tok, const int *pos, int batch, const w
         const wh_bf16 *ckv = cross_kv + (size_t)l * layer_cross;
         // causal self-attention: this token's k / v go to row pos of the caches, then its
         // query attends over rows 0 .. pos
-        if ((rc = ln(Lw.ln1_g, Lw.ln1_b))) return rc;
-        if ((rc = gemm(SK_QKV, xn, d, Lw.wq, Lw.wk, Lw.wv, d, 3 * d, Lw.bq, nullptr, Lw.bv, q, kc, vc))) return rc;
+        if ((rc = gemm(SK_QKV, Lw.ln1_g, Lw.ln1_b, xn, d, Lw.wq, Lw.wk, Lw.wv, d, 3 * d, Lw.bq, nullptr, Lw.bv, q, kc,
+                       vc)))
+            return rc;
         if ((rc = attend(q, kc, vc, d, (long long)cap * d, n_self, cap, da_self))) return rc;
-        if ((rc = gemm(SK_RESID, ao, d, Lw.wo, nullptr, nullptr, d, d, Lw.bo, nullptr, nullptr, x, nullptr, nullptr)))
+        if ((rc = gemm(SK_RESID, nullptr, nullptr, ao, d, Lw.wo, nullptr, nullptr, d, d, Lw.bo, nullptr, nullptr, x,
+                       nullptr, nullptr)))
             return rc;
         // cross-attention into the encoder memory (keys / values cached once per clip)
-        if ((rc = ln(Lw.lnx_g, Lw.lnx_b))) return rc;
-        if ((rc = gemm(SK_BF16, xn, d, Lw.xwq, nullptr, nullptr, d, d, Lw.xbq, nullptr, nullptr, q, nullptr, nullptr)))
+        if ((rc = gemm(SK_BF16, Lw.lnx_g, Lw.lnx_b, xn, d, Lw.xwq, nullptr, nullptr, d, d, Lw.xbq, nullptr, nullptr, q,
+                       nullptr, nullptr)))
             return rc;
         if ((rc = attend(q, ckv, ckv + d, 2LL * d, (long long)n_ctx * 2 * d, nullptr, n_ctx, da_cross))) return rc;
-        if ((rc = gemm(SK_RESID, ao, d, Lw.xwo, nullptr, nullptr, d, d, Lw.xbo, nullptr, nullptr, x, nullptr,
-                       nullptr)))
+        if ((rc = gemm(SK_RESID, nullptr, nullptr, ao, d, Lw.xwo, nullptr, nullptr, d, d, Lw.xbo, nullptr, nullptr, x,
+                       nullptr, nullptr)))
             return rc;
         // feed-forward
-        if ((rc = ln(Lw.ln2_g, Lw.ln2_b))) return rc;
-        if ((rc = gemm(SK_GELU, xn, d, Lw.w1, nullptr, nullptr, f, f, Lw.b1, nullptr, nullptr, hb, nullptr, nullptr)))
+        if ((rc = gemm(SK_GELU, Lw.ln2_g, Lw.ln2_b, xn, d, Lw.w1, nullptr, nullptr, f, f, Lw.b1, nullptr, nullptr, hb,
+                       nullptr, nullptr)))
             return rc;
-        if ((rc = gemm(SK_RESID, hb, f, Lw.w2, nullptr, nullptr, d, d, Lw.b2, nullptr, nullptr, x, nullptr, nullptr)))
+        if ((rc = gemm(SK_RESID, nullptr, nullptr, hb, f, Lw.w2, nullptr, nullptr, d, d, Lw.b2, nullptr, nullptr, x,
+                       nullptr, nullptr)))
             return rc;
     }
     // final norm, logits through the token embedding, greedy token
-    if ((rc = ln(w->lnf_g, w->lnf_b))) return rc;
-    if ((rc = gemm(SK_LOGITS, xn, d, w->tok_embd, nullptr, nullptr, V, V, nullptr, nullptr, nullptr, logits, nullptr,
-                   nullptr)))
+    if ((rc = gemm(SK_LOGITS, w->lnf_g, w->lnf_b, xn, d, w->tok_embd, nullptr, nullptr, V, V, nullptr, nullptr,
+                   nullptr, logits, nullptr, nullptr)))
         return rc;
     if (next_tok) {
         trace_begin(TR_DEC_OTHER, s);
