@@ -44,6 +44,10 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-next", action="store_true", help="skip the cross_kv / audio_ctx measurements")
+    p.add_argument("--decode-only", action="store_true",
+                   help="time only the decoder step (replayed), e.g. to profile it")
+    p.add_argument("--decode-layers", type=int, default=None,
+                   help="with --decode-only: decoder layers (default: as many as the encoder)")
     return p.parse_args()
 
 
@@ -602,10 +606,51 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_decode_only(args):
+    """The decoder step of the workload alone: cross K/V of random bf16 values N(0, 0.5), the
+    step recorded once and replayed `steps` times after `warmup` replays.  Prints one JSON
+    line; for profiling the step's kernels, not a bench line."""
+    import dataclasses
+
+    import torch
+
+    from whisper_audio_encoder_gb300 import build, configs, wh
+    build.build()
+    cfg = configs.CONFIGS[args.config]
+    if args.decode_layers is not None:
+        cfg = dataclasses.replace(cfg, n_layer=args.decode_layers)
+    B, d = cfg.batch, cfg.d_model
+    g = torch.Generator(device="cuda").manual_seed(5)
+    kv = (0.5 * torch.randn(cfg.n_layer, B * 1500, 2 * d, device="cuda", generator=g)).to(torch.bfloat16)
+    dec = wh.Decoder(cfg.n_head, _decoder_weights_on_device(cfg), B)
+    tok = torch.randint(0, cfg.n_vocab, (B,), dtype=torch.int32, device="cuda", generator=g)
+    pos = torch.full((B,), 224, dtype=torch.int32, device="cuda")
+    gs = torch.cuda.Stream()
+    graph = dec.capture(tok, pos, kv, 1500, gs)
+    for _ in range(args.warmup):
+        graph.launch(gs)
+    gs.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(gs)
+    for _ in range(args.steps):
+        graph.launch(gs)
+    e1.record(gs)
+    gs.synchronize()
+    graph.destroy()
+    st = wh.wh_status()
+    if st != wh.WH_OK:
+        raise RuntimeError(f"device status after the decode step: {wh.wh_strerror(st)}")
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    print(json.dumps({"decode_step_only": {"us_per_step": _r(ms * 1e3, 1), "layers": cfg.n_layer, "sequences": B,
+                                           "position": 224, "steps": args.steps, "warmup": args.warmup}}), flush=True)
+
+
 def main():
     args = _args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.decode_only:
+        run_decode_only(args)
     else:
         run_ours(args)
 

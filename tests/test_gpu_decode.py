@@ -14,7 +14,8 @@ Cases: several consecutive steps on a growing cache (tiny width, a vocabulary th
 multiple of 128, 37 encoder positions); ragged positions with NaN in every cache row past a
 sequence's position (never read); large-v3 width (d 1280, 20 heads, vocabulary 51866, 1500
 encoder positions, 16 sequences); the full 32-layer large-v3 decoder on sampled sequences;
-out-of-range tokens and positions (WH_EBOUNDS, clamped); bitwise repeatability.
+batches of 1, 17 and 256 sequences; out-of-range tokens and positions (WH_EBOUNDS, clamped);
+bitwise repeatability; a recorded step replayed.
 """
 import numpy as np
 import pytest
@@ -209,3 +210,19 @@ def test_recorded_step_replays_the_direct_call_and_follows_new_tokens():
     assert torch.equal(c.dec.logits, ref[1])
     graph.destroy()
     assert wh.wh_status() == wh.WH_OK
+
+
+@pytest.mark.parametrize("batch", [1, 17, 256])
+def test_batch_sizes_from_one_to_the_maximum(batch):
+    """One sequence; 17 (one past a 16-row MMA column block, so the padded rows of the
+    operand are live); 256, the largest batch (a full 256-column accumulator)."""
+    c = Case(TINY, n_layer=1, n_vocab=700, cap=12, batch=batch, n_ctx=9, seed=12 + batch)
+    rng = np.random.default_rng(batch)
+    positions = rng.integers(0, 12, size=batch)
+    c.prefill(positions, seed=batch)
+    toks = rng.integers(0, 700, size=batch)
+    got, nxt, st = c.step(toks, positions)
+    assert st == wh.WH_OK
+    for b in sorted({0, batch // 2, batch - 1}):
+        c.check(b, got[b], c.oracle(b, toks[b], positions[b]), nxt[b], f"batch {batch}, sequence {b}")
+        c.check_cache_rows(b, positions[b], f"batch {batch}, sequence {b}")

@@ -472,8 +472,11 @@ int dec_gemm_launch(int mode, const void *x, const float *xf, const float *ln_g,
     if (tiles > 2147483647 / 128) return WH_EINVAL;
     // shared memory: the weight ring (with the TMA-loaded X per stage unless LN is fused), the
     // LN-built X of this split's k-blocks, the barriers, and slack for 1024-byte alignment
+    // (after the MMAs the split's partial tile, B x 128 fp32, is staged from offset 0 for the
+    // cluster reduction: the barriers must lie beyond it too)
     a.x_off = SK_STAGES * a.stage_bytes;
     a.bar_off = a.x_off + (ln_in ? a.kb_per * b_pad * 128 : 0);
+    if (splits > 1 && a.bar_off < batch * 128 * 4) a.bar_off = batch * 128 * 4;
     const int smem = a.bar_off + 128 + 1024;
     if (smem > sk_smem_bytes(SK_MAX_B)) return WH_ENOSPC;
     cudaError_t e;
