@@ -311,45 +311,51 @@ __global__ void __launch_bounds__(THREADS, 1) k_attention_tc(const __grid_consta
                         tmem_wait_st();
                     }
                 }
+                // Scale and subtract the maximum (packed fp32, two keys per instruction) before
+                // this tile's turn, so the turn holds only the exponentials and the P store.
+                const float mc = m * sl2;
+                const uint64_t sl2x2 = f2_pack(sl2, sl2), nmcx2 = f2_pack(-mc, -mc);
+                uint64_t xv[64];                                   // key pairs 2k, 2k + 1
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2)
+                        xv[16 * c + (i >> 1)] =
+                            fma_f2(f2_pack(__uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1])), sl2x2, nmcx2);
                 // Ping-pong: the two tiles take turns in the exponential section, so one tile's
-                // S load, row maximum and waits overlap the other tile's exponentials.
+                // S load, row maximum, scaling, row sum and waits overlap the other tile's
+                // exponentials.
                 ok = __all_sync(0xffffffffu, mbar_wait(turn + t, par, p.ctl));
                 if (!ok) break;
-                const float mc = m * sl2;
-                // exponentials: scale-and-subtract and the row sum two lanes at a time (packed fp32)
-                const uint64_t sl2x2 = f2_pack(sl2, sl2), nmcx2 = f2_pack(-mc, -mc);
-                uint64_t ps[4];                                    // 4 x 2 independent partial sums
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) ps[kk] = 0ull;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {                   // 64 keys -> 32 packed bf16 pairs
                     uint32_t pk[32];
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * hh + cc;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const uint64_t x = fma_f2(f2_pack(__uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1])),
-                                                      sl2x2, nmcx2);
-                            float x0, x1;
-                            f2_unpack(x, x0, x1);
-                            const float e0 = ex2(x0), e1 = ex2(x1);
-                            ps[(i >> 1) & 3] = add_f2(ps[(i >> 1) & 3], f2_pack(e0, e1));
-                            pk[16 * cc + (i >> 1)] = pack_bf16(e0, e1);
-                        }
+                    for (int k = 0; k < 32; ++k) {
+                        float x0, x1;
+                        f2_unpack(xv[32 * hh + k], x0, x1);
+                        const float e0 = ex2(x0), e1 = ex2(x1);
+                        xv[32 * hh + k] = f2_pack(e0, e1);
+                        pk[k] = pack_bf16(e0, e1);
                     }
                     tmem_st32(tP + 32u * hh, pk);
                 }
                 __syncwarp();
                 // tile 1's very last step is the CTA's last turn
                 if (lane == 0 && (t == 0 || !(last_item && j + 1 == nkv))) mbar_arrive(turn + (1 - t));
-                tmem_wait_st();
                 {
+                    // row sum of the exponentials: 4 x 2 independent partial sums, keys in order
+                    uint64_t ps[4];
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) ps[kk] = 0ull;
+#pragma unroll
+                    for (int k = 0; k < 64; ++k) ps[k & 3] = add_f2(ps[k & 3], xv[k]);
                     const uint64_t s2 = add_f2(add_f2(ps[0], ps[1]), add_f2(ps[2], ps[3]));
                     float a0, a1;
                     f2_unpack(s2, a0, a1);
                     l += a0 + a1;
                 }
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full + t);
