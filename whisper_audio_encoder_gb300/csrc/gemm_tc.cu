@@ -30,6 +30,7 @@ namespace {
 constexpr int BK = 64;
 constexpr int GEMM_THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
 constexpr int EPI_WARPS = 8;
+constexpr int GEMM_SK_MIN_KB = 64;   // stream-K only for k-loops of at least this many k-blocks
 
 struct GemmArgs {
     int M, N, num_kb, tiles_n, num_tiles, seg_n;
@@ -38,11 +39,57 @@ struct GemmArgs {
     long long ldo;
     const float *pos;
     int rows_per_win;
+    // Stream-K (residual mode): the first sk_first tiles go round-robin in whole rounds; the
+    // W = (num_tiles - sk_first) * num_kb k-blocks of the rest are shared out in tile order,
+    // pair p of P taking [p W / P, (p + 1) W / P), so every pair gets the same work.  A tile
+    // cut by a pair boundary b is summed by pairs b - 1 (its lower k-blocks, at the end of that
+    // pair's share) and b (its upper k-blocks, first in its share); both write their fp32
+    // partial to slot b of the workspace (tmB.w), and the second to arrive (an atomic ticket
+    // per slot, CTA and epilogue warp; nothing waits) adds the two, the bias and the residual.
+    int sk, sk_first;
+    long long sk_total;
+    int *sk_tickets;  // [slot][CTA of the pair][epilogue warp], zero between launches
     DevCtl ctl;
 };
 
 struct TmapB {
     CUtensorMap m[3];
+    CUtensorMap w;  // stream-K partials: fp32 [slot][2 parts][256 rows][BN], 32 x 32 boxes
+};
+
+// The k-block segments one CTA pair computes, in order: whole tiles pair, pair + P, ... or,
+// with stream-K, the tile pieces of its share.  Producer, MMA issuer and epilogue walk the same
+// sequence.
+struct Walk {
+    long long g, g1;
+    int next_tile, npairs, sk, rr_end;
+    __device__ __forceinline__ Walk(const GemmArgs &p, int pair, int np) : npairs(np), sk(p.sk) {
+        next_tile = pair;
+        rr_end = sk ? p.sk_first : p.num_tiles;
+        const long long base = (long long)p.sk_first * p.num_kb;
+        g = sk ? base + (long long)pair * p.sk_total / np : 0;
+        g1 = sk ? base + (long long)(pair + 1) * p.sk_total / np : 0;
+    }
+    __device__ __forceinline__ bool next(const GemmArgs &p, int &tile, int &kb0, int &kb1) {
+        if (next_tile < rr_end) {
+            tile = next_tile;
+            kb0 = 0;
+            kb1 = p.num_kb;
+            next_tile += npairs;
+            return true;
+        }
+        if (sk) {
+            if (g >= g1) return false;
+            tile = (int)(g / p.num_kb);
+            const long long t0 = (long long)tile * p.num_kb;
+            const long long end = g1 < t0 + p.num_kb ? g1 : t0 + p.num_kb;
+            kb0 = (int)(g - t0);
+            kb1 = (int)(end - t0);
+            g = end;
+            return true;
+        }
+        return false;
+    }
 };
 
 template <int MODE>
@@ -175,6 +222,142 @@ __device__ __forceinline__ void bias_act(const GemmArgs &p, int col, const uint3
     }
 }
 
+// Orders this thread's completed bulk-async (TMA) global accesses with its later generic
+// ones, and the other way round.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Epilogue of a stream-K piece of a tile (residual mode), for this warp's 32 rows x BN / 2
+// columns.  The raw fp32 sum over the piece's k-blocks goes to its half of the slot through
+// the staging tile; once those stores are complete the warp takes the ticket.  The first warp
+// to arrive hands its accumulator back and is done.  The second adds the other half's partial
+// (a + b: the same bits whichever half is its own), then the bias, into the residual stream.
+// Returns false if a wait ran out.
+template <int BN>
+__device__ __forceinline__ bool sk_epilogue(const GemmArgs &p, const CUtensorMap *tmW, const CUtensorMap *tmOut,
+                                            uint8_t *ebuf, uint64_t *xb, uint32_t &xphase, uint32_t tbase,
+                                            uint32_t tempty_remote, int slot, int part, int wrow_base, int row0,
+                                            int colw, int col, int *ticket, int lane) {
+    const int sw = lane & 7;
+    uint8_t *mine = ebuf + lane * 128;
+    const int wrow = wrow_base + part * 256, orow = wrow_base + (1 - part) * 256;
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 64) {
+        if (lane == 0) bulk_wait_read0();  // the previous store has finished reading ebuf
+        __syncwarp();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tbase + (uint32_t)c, r0);
+        tmem_ld32(tbase + (uint32_t)c + 32u, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            *reinterpret_cast<uint4 *>(mine + ((j ^ sw) << 4)) = make_uint4(r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
+            *reinterpret_cast<uint4 *>(mine + 4096 + ((j ^ sw) << 4)) =
+                make_uint4(r1[4 * j], r1[4 * j + 1], r1[4 * j + 2], r1[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmW, ebuf, colw + c, wrow);
+            tma_store_2d(tmW, ebuf + 4096, colw + c + 32, wrow);
+            bulk_commit();
+        }
+    }
+    int t = 0;
+    if (lane == 0) {
+        bulk_wait0();  // this half's partial is in global memory
+        fence_proxy_async_global();
+        __threadfence();
+        t = atomicAdd(ticket, 1);
+    }
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t == 0) {  // the other half will finish the tile
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_remote);
+        return true;
+    }
+    if (lane == 0) {
+        *ticket = 0;  // both halves have arrived: ready for the next launch
+        __threadfence();
+        fence_proxy_async_global();
+    }
+    __syncwarp();
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 64) {
+        if (lane == 0) {
+            bulk_wait_read0();
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(xb, 2 * 4096);
+            tma_load_2d(ebuf, tmW, xb, colw + c, orow);
+            tma_load_2d(ebuf + 4096, tmW, xb, colw + c + 32, orow);
+        }
+        __syncwarp();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tbase + (uint32_t)c, r0);
+        tmem_ld32(tbase + (uint32_t)c + 32u, r1);
+        tmem_wait_ld();
+        if (c + 64 >= BN / 2) {  // last TMEM read of this piece: hand the accumulator back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_remote);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(xb, xphase, p.ctl))) return false;
+        xphase ^= 1u;
+        float v0[32], v1[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 a = *reinterpret_cast<const float4 *>(mine + ((j ^ sw) << 4));
+            const float4 b = *reinterpret_cast<const float4 *>(mine + 4096 + ((j ^ sw) << 4));
+            v0[4 * j] = __uint_as_float(r0[4 * j]) + a.x;
+            v0[4 * j + 1] = __uint_as_float(r0[4 * j + 1]) + a.y;
+            v0[4 * j + 2] = __uint_as_float(r0[4 * j + 2]) + a.z;
+            v0[4 * j + 3] = __uint_as_float(r0[4 * j + 3]) + a.w;
+            v1[4 * j] = __uint_as_float(r1[4 * j]) + b.x;
+            v1[4 * j + 1] = __uint_as_float(r1[4 * j + 1]) + b.y;
+            v1[4 * j + 2] = __uint_as_float(r1[4 * j + 2]) + b.z;
+            v1[4 * j + 3] = __uint_as_float(r1[4 * j + 3]) + b.w;
+        }
+        if (p.bias0 != nullptr) {
+            const float4 *b0 = reinterpret_cast<const float4 *>(p.bias0 + col + c);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 ba = __ldg(b0 + j), bb = __ldg(b0 + 8 + j);
+                v0[4 * j] += ba.x; v0[4 * j + 1] += ba.y; v0[4 * j + 2] += ba.z; v0[4 * j + 3] += ba.w;
+                v1[4 * j] += bb.x; v1[4 * j + 1] += bb.y; v1[4 * j + 2] += bb.z; v1[4 * j + 3] += bb.w;
+            }
+        }
+        fence_proxy_async_smem();  // every lane has read the partial before the residual tile replaces it
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive_expect_tx(xb, 2 * 4096);
+            tma_load_2d(ebuf, tmOut, xb, col + c, row0);
+            tma_load_2d(ebuf + 4096, tmOut, xb, col + c + 32, row0);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(xb, xphase, p.ctl))) return false;
+        xphase ^= 1u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 *a = reinterpret_cast<float4 *>(mine + ((j ^ sw) << 4));
+            float4 *b = reinterpret_cast<float4 *>(mine + 4096 + ((j ^ sw) << 4));
+            float4 xa = *a, xv = *b;
+            xa.x += v0[4 * j]; xa.y += v0[4 * j + 1]; xa.z += v0[4 * j + 2]; xa.w += v0[4 * j + 3];
+            xv.x += v1[4 * j]; xv.y += v1[4 * j + 1]; xv.z += v1[4 * j + 2]; xv.w += v1[4 * j + 3];
+            *a = xa;
+            *b = xv;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmOut, ebuf, col + c, row0);
+            tma_store_2d(tmOut, ebuf + 4096, col + c + 32, row0);
+            bulk_commit();
+        }
+    }
+    return true;
+}
+
 template <int BN, int MODE>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TmapB tmB,
@@ -228,11 +411,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int stage = 0;
         uint32_t phase = 0, issued = 0, last_parity = 0;
         bool ok = true;
-        for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        Walk wk(p, pair, npairs);
+        int tile, kb0, kb1;
+        while (ok && wk.next(p, tile, kb0, kb1)) {
             const int mb = tile / p.tiles_n, nb = tile - mb * p.tiles_n;
             const int n0 = nb * BN, seg = n0 / p.seg_n, nin = n0 - seg * p.seg_n;
             const CUtensorMap *mapB = &tmB.m[seg];
-            for (int kb = 0; kb < p.num_kb; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (*abort_flag || !mbar_wait(empty + stage, phase ^ 1u, p.ctl)) {
                     ok = false;
                     break;
@@ -263,14 +448,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool ok = true;
-        for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+        Walk wk(p, pair, npairs);
+        int tile, kb0, kb1;
+        while (ok && wk.next(p, tile, kb0, kb1)) {
             if (*abort_flag || !mbar_wait(tempty + acc, acc_phase ^ 1u, p.ctl)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < p.num_kb; ++kb) {
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (*abort_flag || !mbar_wait(full + stage, phase, p.ctl)) {
                     ok = false;
                     break;
@@ -281,7 +468,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
                     umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), IDESC,
-                                   (kb | k) != 0 ? 1u : 0u);
+                                   (kb != kb0 || k != 0) ? 1u : 0u);
                 umma_commit_pair(empty + stage, 0x3);  // frees the stage in both CTAs
                 if (++stage == C::STAGES) {
                     stage = 0;
@@ -313,7 +500,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int tile = pair; tile < p.num_tiles; tile += npairs) {
+        Walk wk(p, pair, npairs);
+        int tile, kb0, kb1;
+        while (wk.next(p, tile, kb0, kb1)) {
             ok = !*abort_flag && mbar_wait(tfull + acc, acc_phase, p.ctl);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
@@ -325,6 +514,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int row0 = mb * 256 + (int)rank * 128 + q * 32, row = row0 + lane;
             const int c0 = half * (BN / 2);
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0);
+            if constexpr (MODE == GEMM_RESID_F32) {
+                if (kb0 > 0 || kb1 < p.num_kb) {  // a stream-K piece of a tile cut by a pair boundary
+                    const int slot = kb0 > 0 ? pair : pair + 1, part = kb0 > 0 ? 1 : 0;
+                    ok = sk_epilogue<BN>(p, &tmB.w, &tmOut, ebuf, xb, xphase, tbase,
+                                         tempty_leader0 + (uint32_t)(acc * 8), slot, part,
+                                         slot * 512 + (int)rank * 128 + q * 32, row0, c0, nb * BN + c0,
+                                         p.sk_tickets + (slot * 2 + (int)rank) * EPI_WARPS + ew, lane);
+                    if (!ok) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    if (++acc == 2) {
+                        acc = 0;
+                        acc_phase ^= 1u;
+                    }
+                    continue;
+                }
+            }
 #pragma unroll 1
             for (int c = 0; c < BN / 2; c += 64) {
                 const int col = nb * BN + c0 + c;
@@ -582,6 +789,31 @@ int gemm_launch(const GemmDesc &g, int mode, const DevCtl &ctl, int num_sms, cud
     }
     const int resident = BN == 256 ? max_active_pairs<256>(num_sms) : max_active_pairs<128>(num_sms);
     const int pairs = a.num_tiles < resident ? a.num_tiles : resident;
+    // Stream-K for the residual mode when the tiles do not fill whole rounds: every pair's share
+    // (at least one tile's k-blocks, so a cut tile has exactly two pieces) ends within one tile
+    // of every other pair's, instead of some pairs running one tile more than the rest.
+    a.sk = 0;
+    a.sk_first = 0;
+    a.sk_total = 0;
+    a.sk_tickets = g.sk_tickets;
+    tb.w = tb.m[0];
+    // Only for long k-loops (fc2): with a short one (out_proj, K = d) the two partial writes and
+    // the second piece's reloads cost more than the balance saves.
+    if (mode == GEMM_RESID_F32 && g.sk_ws != nullptr && g.sk_tickets != nullptr && a.num_tiles > pairs &&
+        a.num_tiles % pairs != 0 && a.num_kb >= GEMM_SK_MIN_KB && pairs + 1 <= g.sk_slots &&
+        g.sk_slots <= GEMM_SK_SLOTS) {
+        // whole rounds but the last go round-robin (neighbouring pairs on neighbouring tiles, so
+        // operands are shared in L2); the last whole round and the remainder are shared out,
+        // at least one tile's k-blocks per pair
+        const int first = (a.num_tiles / pairs - 1) * pairs;
+        const long long total = (long long)(a.num_tiles - first) * a.num_kb;
+        if (total / pairs >= a.num_kb) {
+            if (int rc = make_tmap_f32(&tb.w, g.sk_ws, (long long)g.sk_slots * 512, BN, BN, 32)) return rc;
+            a.sk = 1;
+            a.sk_first = first;
+            a.sk_total = total;
+        }
+    }
     count_launch();
     return BN == 256 ? launch_pair_mode<256>(mode, ta, tb, to, a, 2 * pairs, s)
                      : launch_pair_mode<128>(mode, ta, tb, to, a, 2 * pairs, s);

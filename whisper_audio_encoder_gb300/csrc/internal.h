@@ -26,7 +26,24 @@ struct GemmDesc {
     void *out; long long ldo;             // output (elements)
     const float *pos;                     // GEMM_CONV2: [rows_per_win][N]
     int rows_per_win;                     // GEMM_CONV1: c1 frames per window; GEMM_CONV2: positions
+    // GEMM_RESID_F32, optional (null: whole tiles only): scratch for stream-K with room for
+    // sk_slots pair boundaries (gemm_sk_bytes), and sk_slots * 2 * 8 ints that are zero before
+    // the first launch (each launch leaves them zero)
+    void *sk_ws;
+    int *sk_tickets;
+    int sk_slots;
 };
+constexpr int GEMM_SK_SLOTS = 128;   // pair boundaries the scratch holds at most
+// Stream-K slots worth keeping for a residual GEMM of M rows and N = ldo columns, and their bytes.
+inline int gemm_sk_slots(long long M, int N) {
+    const int bn = N % 256 == 0 ? 256 : 128;
+    const long long tiles = (M + 255) / 256 * (N / bn) + 1;
+    return (int)(tiles < GEMM_SK_SLOTS ? tiles : GEMM_SK_SLOTS);
+}
+inline size_t gemm_sk_bytes(long long M, int N) {
+    return (size_t)gemm_sk_slots(M, N) * 2 * 256 * (N % 256 == 0 ? 256 : 128) * 4;
+}
+inline size_t gemm_sk_ticket_bytes(long long M, int N) { return (size_t)gemm_sk_slots(M, N) * 2 * 8 * 4; }
 // 2-D bf16 TMA descriptor: rows x cols (row stride ld elements), box 64 x box_rows, 128-byte
 // swizzle, zero fill outside.  Returns a WH_* code.
 int make_tmap_bf16(CUtensorMap *m, const void *ptr, long long rows, int cols, int ld, int box_rows);

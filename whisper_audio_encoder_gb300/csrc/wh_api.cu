@@ -116,7 +116,7 @@ int check_config(const wh_config *c) {
 }
 
 struct EncLayout {
-    size_t x, xn, qkv, ao, h, a1, w1p, w2p, total;
+    size_t x, xn, qkv, ao, h, a1, w1p, w2p, sk, skt, total;
 };
 
 // n_ctx encoder positions per window (conv1 runs over 2 n_ctx log-mel frames)
@@ -132,6 +132,8 @@ EncLayout layout(const wh_config *c, int batch, int n_ctx) {
     L.a1 = off;  off += up256((size_t)batch * 2 * n_ctx * 3 * M * 2);
     L.w1p = off; off += up256(d * 3 * M * 2);
     L.w2p = off; off += up256(d * 3 * d * 2);
+    L.sk = off;  off += up256(gemm_sk_bytes((long long)rows, (int)d));   // stream-K partials of out_proj / fc2
+    L.skt = off; off += up256(gemm_sk_ticket_bytes((long long)rows, (int)d));
     L.total = off;
     return L;
 }
@@ -349,7 +351,10 @@ int wh_encode_ctx(const float *mel, int batch, int n_ctx, const wh_config *cfg, 
     float *x = reinterpret_cast<float *>(ws + L.x);
     void *xn = ws + L.xn, *qkv = ws + L.qkv, *ao = ws + L.ao, *hb = ws + L.h, *a1 = ws + L.a1;
     void *w1p = ws + L.w1p, *w2p = ws + L.w2p;
+    int *sk_tickets = reinterpret_cast<int *>(ws + L.skt);
     int rc;
+    const int sk_slots = gemm_sk_slots((long long)rows, d);
+    if (cudaMemsetAsync(sk_tickets, 0, gemm_sk_ticket_bytes((long long)rows, d), s) != cudaSuccess) return WH_ECUDA;
 
     // ---- conv stem over the first 2 n_ctx frames of each window
     trace_begin(TR_STEM_PREP, s);
@@ -386,15 +391,25 @@ int wh_encode_ctx(const float *mel, int batch, int n_ctx, const wh_config *cfg, 
         trace_begin(TR_ATTN, s);
         if ((rc = attention_launch(qkv, batch, n_ctx, H, ao, ctl_of(st), st->num_sms, s))) return rc;
         trace_end(TR_ATTN, s, 4.0 * batch * (double)n_ctx * n_ctx * d, (double)rows * d * 8.0);
-        if ((rc = run_gemm(gemm(ao, d, rows, d, Lw.wo, d, d, Lw.bo, x, d), GEMM_RESID_F32, st, s, TR_GEMM_OUT)))
-            return rc;
+        {
+            GemmDesc g = gemm(ao, d, rows, d, Lw.wo, d, d, Lw.bo, x, d);
+            g.sk_ws = ws + L.sk;
+            g.sk_tickets = sk_tickets;
+            g.sk_slots = sk_slots;
+            if ((rc = run_gemm(g, GEMM_RESID_F32, st, s, TR_GEMM_OUT))) return rc;
+        }
         trace_begin(TR_LAYERNORM, s);
         if ((rc = layernorm_launch(x, rows, d, Lw.ln2_g, Lw.ln2_b, xn, 1, s))) return rc;
         trace_end(TR_LAYERNORM, s, 0.0, (double)rows * d * 6.0);
         if ((rc = run_gemm(gemm(xn, d, rows, d, Lw.w1, d, f, Lw.b1, hb, f), GEMM_GELU_BF16, st, s, TR_GEMM_FC1)))
             return rc;
-        if ((rc = run_gemm(gemm(hb, f, rows, f, Lw.w2, f, d, Lw.b2, x, d), GEMM_RESID_F32, st, s, TR_GEMM_FC2)))
-            return rc;
+        {
+            GemmDesc g = gemm(hb, f, rows, f, Lw.w2, f, d, Lw.b2, x, d);
+            g.sk_ws = ws + L.sk;
+            g.sk_tickets = sk_tickets;
+            g.sk_slots = sk_slots;
+            if ((rc = run_gemm(g, GEMM_RESID_F32, st, s, TR_GEMM_FC2))) return rc;
+        }
     }
     trace_begin(TR_LAYERNORM, s);
     rc = layernorm_launch(x, rows, d, w->lnf_g, w->lnf_b, out, 0, s);
