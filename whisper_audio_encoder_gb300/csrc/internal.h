@@ -65,9 +65,10 @@ int frontend_ctl(DevCtl *ctl, int *num_sms);   // the current device's control b
 
 // ---- other kernels ---------------------------------------------------------------------
 // pdl: launched with programmatic stream serialization (may start before the previous kernel
-// has finished; waits for it before reading x)
+// has finished; waits for it before reading x).  reverse: rows are taken from the last one
+// down (after a kernel that stored them in ascending order, its last rows are still in L2).
 int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,
-                     cudaStream_t s, bool pdl = false);
+                     cudaStream_t s, bool pdl = false, bool reverse = false);
 int attention_launch(const void *qkv, int batch, int n_ctx, int n_head, void *out, const DevCtl &ctl,
                      int num_sms, cudaStream_t s);
 int attention_prepare();

@@ -16,16 +16,20 @@ constexpr int MAXV = 16;  // float4 per lane: d <= 2048
 // d a multiple of 128: each lane holds d / 128 float4 (16-byte loads and stores).  NV > 0
 // fixes d = 128 NV at compile time (registers sized to the row: more rows in flight per SM);
 // NV = 0 takes d at run time (up to MAXV float4 per lane).
+// reverse: blocks take the rows from the last one down (the rows a GEMM stored last are the ones
+// still in L2).
 template <int NV, bool OUT_BF16>
 __global__ void __launch_bounds__(LN_THREADS) k_layernorm(const float *__restrict__ x, int rows, int d,
                                                           const float *__restrict__ g,
-                                                          const float *__restrict__ b, void *__restrict__ y) {
+                                                          const float *__restrict__ b, void *__restrict__ y,
+                                                          int reverse) {
     constexpr int CAP = NV > 0 ? NV : MAXV;
-    const int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
+    int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     pdl_launch_dependents();
     pdl_wait();
     if (row >= rows) return;
+    if (reverse) row = rows - 1 - row;
     const int nv = NV > 0 ? NV : d >> 7;
     if (NV > 0) d = NV * 128;
     const float4 *xr = reinterpret_cast<const float4 *>(x + (long long)row * d);
@@ -85,23 +89,25 @@ cudaLaunchConfig_t ln_config(int grid, cudaStream_t s, bool pdl, cudaLaunchAttri
 
 template <int NV>
 cudaError_t launch_ln(int grid, cudaStream_t s, bool pdl, const float *x, int rows, int d, const float *g,
-                      const float *b, void *y, int y_bf16) {
+                      const float *b, void *y, int y_bf16, int rev) {
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t lc = ln_config(grid, s, pdl, attr);
-    return y_bf16 ? cudaLaunchKernelEx(&lc, k_layernorm<NV, true>, x, rows, d, g, b, y)
-                  : cudaLaunchKernelEx(&lc, k_layernorm<NV, false>, x, rows, d, g, b, y);
+    return y_bf16 ? cudaLaunchKernelEx(&lc, k_layernorm<NV, true>, x, rows, d, g, b, y, rev)
+                  : cudaLaunchKernelEx(&lc, k_layernorm<NV, false>, x, rows, d, g, b, y, rev);
 }
 
 // d a multiple of 64 but not of 128: float2 per lane.
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(LN_THREADS) k_layernorm64(const float *__restrict__ x, int rows, int d,
                                                             const float *__restrict__ g,
-                                                            const float *__restrict__ b, void *__restrict__ y) {
-    const int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
+                                                            const float *__restrict__ b, void *__restrict__ y,
+                                                            int reverse) {
+    int row = blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     pdl_launch_dependents();
     pdl_wait();
     if (row >= rows) return;
+    if (reverse) row = rows - 1 - row;
     const int nv = d >> 6;
     const float2 *xr = reinterpret_cast<const float2 *>(x + (long long)row * d);
     float2 v[2 * MAXV];
@@ -141,25 +147,26 @@ __global__ void __launch_bounds__(LN_THREADS) k_layernorm64(const float *__restr
 }  // namespace
 
 int layernorm_launch(const float *x, int rows, int d, const float *g, const float *b, void *y, int y_bf16,
-                     cudaStream_t s, bool pdl) {
+                     cudaStream_t s, bool pdl, bool reverse) {
+    const int rev = reverse ? 1 : 0;
     if (rows <= 0) return WH_OK;
     if (d % 64 != 0 || d < 64 || d > 128 * MAXV) return WH_EINVAL;
     const int grid = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
     cudaError_t e;
     if (d % 128 == 0) {
         switch (d / 128) {  // the family's widths (384, 512, 768, 1024, 1280) get exact registers
-            case 3: e = launch_ln<3>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
-            case 4: e = launch_ln<4>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
-            case 6: e = launch_ln<6>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
-            case 8: e = launch_ln<8>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
-            case 10: e = launch_ln<10>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
-            default: e = launch_ln<0>(grid, s, pdl, x, rows, d, g, b, y, y_bf16); break;
+            case 3: e = launch_ln<3>(grid, s, pdl, x, rows, d, g, b, y, y_bf16, rev); break;
+            case 4: e = launch_ln<4>(grid, s, pdl, x, rows, d, g, b, y, y_bf16, rev); break;
+            case 6: e = launch_ln<6>(grid, s, pdl, x, rows, d, g, b, y, y_bf16, rev); break;
+            case 8: e = launch_ln<8>(grid, s, pdl, x, rows, d, g, b, y, y_bf16, rev); break;
+            case 10: e = launch_ln<10>(grid, s, pdl, x, rows, d, g, b, y, y_bf16, rev); break;
+            default: e = launch_ln<0>(grid, s, pdl, x, rows, d, g, b, y, y_bf16, rev); break;
         }
     } else {
         cudaLaunchAttribute attr[1];
         const cudaLaunchConfig_t lc = ln_config(grid, s, pdl, attr);
-        e = y_bf16 ? cudaLaunchKernelEx(&lc, k_layernorm64<true>, x, rows, d, g, b, y)
-                   : cudaLaunchKernelEx(&lc, k_layernorm64<false>, x, rows, d, g, b, y);
+        e = y_bf16 ? cudaLaunchKernelEx(&lc, k_layernorm64<true>, x, rows, d, g, b, y, rev)
+                   : cudaLaunchKernelEx(&lc, k_layernorm64<false>, x, rows, d, g, b, y, rev);
     }
     count_launch();
     return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? WH_OK : WH_ECUDA;

@@ -377,7 +377,7 @@ int wh_encode_ctx(const float *mel, int batch, int n_ctx, const wh_config *cfg, 
     for (int l = 0; l < cfg->n_layer; ++l) {
         const wh_layer_weights &Lw = w->layers[l];
         trace_begin(TR_LAYERNORM, s);
-        if ((rc = layernorm_launch(x, rows, d, Lw.ln1_g, Lw.ln1_b, xn, 1, s))) return rc;
+        if ((rc = layernorm_launch(x, rows, d, Lw.ln1_g, Lw.ln1_b, xn, 1, s, false, true))) return rc;
         trace_end(TR_LAYERNORM, s, 0.0, (double)rows * d * 6.0);
         {
             GemmDesc g = gemm(xn, d, rows, d, Lw.wq, d, 3 * d, Lw.bq, qkv, 3LL * d);
@@ -399,7 +399,7 @@ int wh_encode_ctx(const float *mel, int batch, int n_ctx, const wh_config *cfg, 
             if ((rc = run_gemm(g, GEMM_RESID_F32, st, s, TR_GEMM_OUT))) return rc;
         }
         trace_begin(TR_LAYERNORM, s);
-        if ((rc = layernorm_launch(x, rows, d, Lw.ln2_g, Lw.ln2_b, xn, 1, s))) return rc;
+        if ((rc = layernorm_launch(x, rows, d, Lw.ln2_g, Lw.ln2_b, xn, 1, s, false, true))) return rc;
         trace_end(TR_LAYERNORM, s, 0.0, (double)rows * d * 6.0);
         if ((rc = run_gemm(gemm(xn, d, rows, d, Lw.w1, d, f, Lw.b1, hb, f), GEMM_GELU_BF16, st, s, TR_GEMM_FC1)))
             return rc;
@@ -412,7 +412,7 @@ int wh_encode_ctx(const float *mel, int batch, int n_ctx, const wh_config *cfg, 
         }
     }
     trace_begin(TR_LAYERNORM, s);
-    rc = layernorm_launch(x, rows, d, w->lnf_g, w->lnf_b, out, 0, s);
+    rc = layernorm_launch(x, rows, d, w->lnf_g, w->lnf_b, out, 0, s, false, true);
     trace_end(TR_LAYERNORM, s, 0.0, (double)rows * d * 8.0);
     return rc;
 }
