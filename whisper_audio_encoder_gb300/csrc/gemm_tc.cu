@@ -18,6 +18,10 @@
 //   warps 2..9  (both CTAs) epilogue on this CTA's 128 rows: tcgen05.ld, bias / GELU /
 //               residual / positions, TMA store through a per-warp staging tile; then hand
 //               the accumulator back so the MMA of tile i+2 can start.
+// Tiles go to the pairs round-robin.  A long-K residual GEMM whose tiles do not fill whole
+// rounds shares the k-blocks of its last rounds evenly between the pairs instead (stream-K,
+// see GemmArgs::sk); a tile cut between two pairs is summed in two pieces and merged by the
+// second to finish, without waiting.
 // Every wait is bounded (DevCtl::wait_ns); on expiry the block records WH_ETIMEOUT, winds
 // down, waits for its own copies and MMAs in flight, frees TMEM and returns.
 #include "common.cuh"
