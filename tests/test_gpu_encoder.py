@@ -120,3 +120,25 @@ def test_stream_k_fc2_is_deterministic_and_matches_whole_tiles():
     assert worst <= ENC_ATOL, f"stream-K vs whole tiles: max |diff| {worst:.3e}"
     _, ref = R.encode_window(pcm[9], w, 128, 20)
     check_encoder(a[9].cpu().numpy(), ref, "window 9")
+
+
+@pytest.mark.parametrize("batch,windows", [(4, [0, 3]), (11, [0, 5, 10])])
+def test_stream_k_shares_without_and_with_round_robin_rounds(batch, windows):
+    """fc2 at large-v3 width, one block: 4 windows are 120 tiles (fewer than two rounds, so every
+    k-block is shared out stream-K); 11 windows are 325 tiles (three round-robin rounds, then
+    the last round and the remainder shared out).  Sampled windows against the oracle, and two
+    runs bitwise equal."""
+    cfg = configs.EncoderConfig(f"sk-b{batch}", 128, 1280, 20, 1, 5120, batch, "speech", index=3)
+    w = synth.random_weights(128, 1280, 1, 5120, seed=80 + batch, ln_random=True)
+    enc = wh.Encoder(cfg, w)
+    pcm = synth.waveforms(cfg)
+    mel = wh.wh_frontend(torch.from_numpy(pcm).cuda(), 128)
+    a = enc.wh_encode(mel).clone()
+    b = enc.wh_encode(mel)
+    torch.cuda.synchronize()
+    assert wh.wh_status() == wh.WH_OK
+    assert torch.equal(a, b)
+    out = a.cpu().numpy()
+    for win in windows:
+        _, ref = R.encode_window(pcm[win], w, 128, 20)
+        check_encoder(out[win], ref, f"batch {batch}, window {win}")
