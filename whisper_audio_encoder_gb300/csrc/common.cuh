@@ -327,6 +327,8 @@ __device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
 // formula 7.1.26 (|error| <= 1.5e-7 for all z >= 0, odd extension for z < 0):
 //   erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),  t = 1 / (1 + p z).
 // The error is far below the bf16 rounding of every output that uses it.
+// With erf(|x| / sqrt 2) = 1 - q e, GELU(x) = max(x, 0) - |x| q e / 2 for either sign (no
+// 1 - (1 - q e) cancellation below zero).
 __device__ __forceinline__ float gelu_erf(float x) {
     const float z = fabsf(x) * 0.70710678118654752f;
     const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));
@@ -334,19 +336,20 @@ __device__ __forceinline__ float gelu_erf(float x) {
     poly = fmaf(t, poly, 1.421413741f);
     poly = fmaf(t, poly, -0.284496736f);
     poly = fmaf(t, poly, 0.254829592f);
-    poly *= t;
-    const float e = ex2_approx(-z * z * 1.4426950408889634f);
-    const float erf_abs = fmaf(-poly, e, 1.0f);
-    return 0.5f * x * (1.0f + copysignf(erf_abs, x));
+    const float r = (poly * t) * (z * -0.70710678118654752f);   // -|x| q / 2
+    const float e = ex2_approx(z * z * -1.4426950408889634f);
+    return fmaf(r, e, fmaxf(x, 0.0f));
 }
 __device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-// GELU of two values at once (same formula as gelu_erf), packed fp32 where it pays.
+// GELU of two values at once (the erf of gelu_erf), packed fp32 where it pays.  With
+// erf(|x| / sqrt 2) = 1 - q e (q = the polynomial times t, e = exp(-x^2 / 2)), GELU is
+// x - x q e / 2 for x >= 0 and x q e / 2 for x < 0, i.e. max(x, 0) - |x| q e / 2: one form for
+// both signs and no 1 - (1 - q e) cancellation below zero.
 __device__ __forceinline__ void gelu_erf2(float &x0, float &x1) {
-    const uint64_t x = f2_pack(x0, x1);
     const uint64_t z = f2_pack(fabsf(x0) * 0.70710678118654752f, fabsf(x1) * 0.70710678118654752f);
     float za, zb;
     f2_unpack(fma_f2(z, f2_pack(0.3275911f, 0.3275911f), f2_pack(1.0f, 1.0f)), za, zb);
@@ -355,15 +358,11 @@ __device__ __forceinline__ void gelu_erf2(float &x0, float &x1) {
     poly = fma_f2(t, poly, f2_pack(1.421413741f, 1.421413741f));
     poly = fma_f2(t, poly, f2_pack(-0.284496736f, -0.284496736f));
     poly = fma_f2(t, poly, f2_pack(0.254829592f, 0.254829592f));
-    poly = mul_f2(poly, t);
+    const uint64_t r = mul_f2(mul_f2(poly, t), mul_f2(z, f2_pack(-0.70710678118654752f, -0.70710678118654752f)));  // -|x| q / 2
     float ea, eb;
     f2_unpack(mul_f2(mul_f2(z, z), f2_pack(-1.4426950408889634f, -1.4426950408889634f)), ea, eb);
     const uint64_t e = f2_pack(ex2_approx(ea), ex2_approx(eb));
-    float ra, rb;  // |erf|
-    f2_unpack(fma_f2(poly, f2_pack(-1.0f, -1.0f) /* -poly */, f2_pack(0.0f, 0.0f)), ra, rb);
-    f2_unpack(fma_f2(f2_pack(ra, rb), e, f2_pack(1.0f, 1.0f)), ra, rb);
-    const uint64_t one_plus = f2_pack(1.0f + copysignf(ra, x0), 1.0f + copysignf(rb, x1));
-    f2_unpack(mul_f2(mul_f2(x, f2_pack(0.5f, 0.5f)), one_plus), x0, x1);
+    f2_unpack(fma_f2(r, e, f2_pack(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f))), x0, x1);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
