@@ -350,17 +350,21 @@ __device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
 // x - x q e / 2 for x >= 0 and x q e / 2 for x < 0, i.e. max(x, 0) - |x| q e / 2: one form for
 // both signs and no 1 - (1 - q e) cancellation below zero.
 __device__ __forceinline__ void gelu_erf2(float &x0, float &x1) {
-    const uint64_t z = f2_pack(fabsf(x0) * 0.70710678118654752f, fabsf(x1) * 0.70710678118654752f);
-    float za, zb;
-    f2_unpack(fma_f2(z, f2_pack(0.3275911f, 0.3275911f), f2_pack(1.0f, 1.0f)), za, zb);
-    const uint64_t t = f2_pack(rcp_approx(za), rcp_approx(zb));
-    uint64_t poly = fma_f2(t, f2_pack(1.061405429f, 1.061405429f), f2_pack(-1.453152027f, -1.453152027f));
-    poly = fma_f2(t, poly, f2_pack(1.421413741f, 1.421413741f));
-    poly = fma_f2(t, poly, f2_pack(-0.284496736f, -0.284496736f));
-    poly = fma_f2(t, poly, f2_pack(0.254829592f, 0.254829592f));
-    const uint64_t r = mul_f2(mul_f2(poly, t), mul_f2(z, f2_pack(-0.70710678118654752f, -0.70710678118654752f)));  // -|x| q / 2
+    // t = 1 / (1 + p |x| / sqrt 2); the polynomial's coefficients carry the -1/2, so
+    // r = poly(t) t |x| = -|x| q / 2 directly; e = 2^(-x^2 log2(e) / 2)
+    const uint64_t x = f2_pack(x0, x1);
+    const uint64_t ax = f2_pack(fabsf(x0), fabsf(x1));
+    float ua, ub;
+    f2_unpack(fma_f2(ax, f2_pack(0.23164188861846924f, 0.23164188861846924f), f2_pack(1.0f, 1.0f)), ua, ub);
+    const uint64_t t = f2_pack(rcp_approx(ua), rcp_approx(ub));
+    uint64_t poly = fma_f2(t, f2_pack(-0.5307027101516724f, -0.5307027101516724f),
+                           f2_pack(0.726576030254364f, 0.726576030254364f));
+    poly = fma_f2(t, poly, f2_pack(-0.710706889629364f, -0.710706889629364f));
+    poly = fma_f2(t, poly, f2_pack(0.14224836230278015f, 0.14224836230278015f));
+    poly = fma_f2(t, poly, f2_pack(-0.1274147927761078f, -0.1274147927761078f));
+    const uint64_t r = mul_f2(mul_f2(poly, t), ax);
     float ea, eb;
-    f2_unpack(mul_f2(mul_f2(z, z), f2_pack(-1.4426950408889634f, -1.4426950408889634f)), ea, eb);
+    f2_unpack(mul_f2(mul_f2(x, x), f2_pack(-0.7213475108146667f, -0.7213475108146667f)), ea, eb);
     const uint64_t e = f2_pack(ex2_approx(ea), ex2_approx(eb));
     f2_unpack(fma_f2(r, e, f2_pack(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f))), x0, x1);
 }

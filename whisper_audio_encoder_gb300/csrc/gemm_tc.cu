@@ -212,12 +212,10 @@ __device__ __forceinline__ void bias_act(const GemmArgs &p, int col, const uint3
     if (bias != nullptr) {
         const float4 *b4 = reinterpret_cast<const float4 *>(bias + (col - seg * p.seg_n));
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 8; ++j) {  // packed pairs
             const float4 b = __ldg(b4 + j);
-            v[4 * j] += b.x;
-            v[4 * j + 1] += b.y;
-            v[4 * j + 2] += b.z;
-            v[4 * j + 3] += b.w;
+            f2_unpack(add_f2(f2_pack(v[4 * j], v[4 * j + 1]), f2_pack(b.x, b.y)), v[4 * j], v[4 * j + 1]);
+            f2_unpack(add_f2(f2_pack(v[4 * j + 2], v[4 * j + 3]), f2_pack(b.z, b.w)), v[4 * j + 2], v[4 * j + 3]);
         }
     }
     if constexpr (MODE == GEMM_GELU_BF16) {
